@@ -1,0 +1,542 @@
+"""Benchmark of the trellis-quantized linear layer on GB300.
+
+Headline workload: the decode-shaped gate_proj geometry (K=5120, N=17408,
+bits=4), one step = four exl3_linear calls at M = 1, 4, 8, 16 (fp16 in,
+fp16 out), weights resident in HBM. Metric: weight GB/s = trellis bytes read
+per step / step time. Twelve rotating weight copies (535 MB, > 4x L2) keep
+every call's weights out of L2. The timed loop replays CUDA graphs of one
+step each.
+
+Also measured in the same run (reported as sub-objects of the JSON line):
+  prefill   - the prefill-shaped call on the same geometry at M=2048
+              (TFLOP/s = 2*M*K*N / call time, reconstruct and Hadamards
+              included), with the reconstruct / GEMM split;
+  crossover - both paths timed at M in {64 .. 4096} on both MLP geometries;
+  logits    - the odd-vocab masked logits call at M in {1, 16, 2048}.
+
+--impl reference times the CPU oracle (test infrastructure) on the host's
+cores on a bounded sample of the same workload, as the reference arm.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       [--quick] [--no-extras]
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "EXL3 linear: decode weight GB/s, prefill TFLOP/s, both as % roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+WEIGHT_COPIES = 12
+
+
+# ---------------------------------------------------------------------------
+# plumbing
+# ---------------------------------------------------------------------------
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--quick", action="store_true", help="smaller extras (for profiling runs)")
+    p.add_argument("--no-extras", action="store_true", help="headline workload only")
+    return p.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; keeps those inside [t0, t1]."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.6)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        time.sleep(0.25)
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        inside, allv = [], []
+        for ln in self.lines:
+            parts = [s.strip() for s in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rec = (ts, float(parts[1]), float(parts[2]), parts[4:9])
+            except ValueError:
+                continue
+            allv.append(rec)
+            if self.t0 is not None and self.t0 - 0.25 <= ts <= (self.t1 or ts) + 0.25:
+                inside.append(rec)
+        use = inside if inside else allv[-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    want = source_hash(kernel_file)
+    rec_hash, traffic = None, None
+    for line in text.splitlines():
+        if line.startswith("source_sha256_16:"):
+            rec_hash = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if rec_hash == want else None
+
+
+# ---------------------------------------------------------------------------
+# device helpers
+# ---------------------------------------------------------------------------
+
+def _dev(torch, a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+class DevMatrix:
+    def __init__(self, torch, mat, n_gemm=None):
+        self.K, self.n_stored, self.bits = mat.K, mat.n_stored, mat.bits
+        self.n_gemm = mat.n_stored if n_gemm is None else n_gemm
+        self.trellis = _dev(torch, mat.trellis)
+        self.su = _dev(torch, mat.su)
+        self.sv = _dev(torch, mat.sv)
+        self.nbytes = mat.trellis.nbytes
+
+
+def make_ws(torch, tql, M_max, K, n_gemm, bits, thr):
+    n = tql.exl3_linear_workspace_bytes(M_max, K, n_gemm, bits, thr)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    tql.exl3_workspace_init(ws)
+    return ws
+
+
+def call_linear(tql, x, M, mat, y, thr, ws, y_dtype):
+    tql.exl3_linear(x, M, mat.K, mat.trellis, mat.bits, mat.n_stored, mat.n_gemm, mat.su, mat.sv, y, y_dtype,
+                    thr, ws)
+
+
+def time_fn(torch, fn, iters, warmup=2):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+# ---------------------------------------------------------------------------
+# headline: decode-shaped gate_proj
+# ---------------------------------------------------------------------------
+
+def bench_decode(args, torch, tql, peaks, dist):
+    world, rank, local = dist
+    g = synthetic.GATE_DECODE
+    K, N, bits, Ms = g["K"], g["N"], g["bits"], g["Ms"]
+    mats = [DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=g["seed"], matrix_index=j))
+            for j in range(WEIGHT_COPIES)]
+    xs = {M: _dev(torch, synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"])) for M in Ms}
+    ys = {M: torch.empty((M, N), dtype=torch.float16, device="cuda") for M in Ms}
+    thr = 128
+    ws = make_ws(torch, tql, max(Ms), K, N, bits, 0)
+    wbytes = mats[0].nbytes
+    per_step_bytes = wbytes * len(Ms)
+
+    stream = torch.cuda.Stream()
+    graphs = []
+    n_graphs = WEIGHT_COPIES // len(Ms)
+    with torch.cuda.stream(stream):
+        # eager warm-up of every shape before capture
+        for i, M in enumerate(Ms):
+            call_linear(tql, xs[M], M, mats[i], ys[M], thr, ws, tql.EXL3_F16)
+        torch.cuda.synchronize()
+        for gi in range(n_graphs):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i, M in enumerate(Ms):
+                    call_linear(tql, xs[M], M, mats[gi * len(Ms) + i], ys[M], thr, ws, tql.EXL3_F16)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_graphs].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_graphs].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = per_step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # per-M kernel durations (graph of 12 back-to-back launches of one shape)
+    per_m = {}
+    for M in Ms:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gr, stream=stream):
+                for j in range(WEIGHT_COPIES):
+                    call_linear(tql, xs[M], M, mats[j], ys[M], thr, ws, tql.EXL3_F16)
+            t_ms = time_fn(torch, gr.replay, 50, 5) / WEIGHT_COPIES
+        per_m[str(M)] = {"us_per_call": round(t_ms * 1e3, 3),
+                         "weight_gbs": round(wbytes / (t_ms * 1e-3) / 1e9, 1)}
+    launch_us = ms_per_step * 1e3 / len(Ms)  # the step is exactly len(Ms) decode-GEMM launches
+    achieved = wbytes / (launch_us * 1e-6) / 1e9
+    return {
+        "value": value, "ms_per_step": ms_per_step, "clocks": clk, "per_m": per_m,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic("trellis_quantized_linear_gb300/csrc/exl3_decode_gemm.cu",
+                                                 "decode_gemm_gate_k5120_n17408_b4.md"),
+                     "peak_kind": f"of {peaks['source']} (burst copy)", "kernel": "decode_gemm_kernel<4,*>",
+                     "bytes_per_launch": wbytes},
+        "gpu_launches": args.steps * len(Ms),
+        "weights_per_step_bytes": per_step_bytes,
+        "mats": mats, "xs": xs, "ws": ws,
+    }
+
+
+def bench_e2e(args, torch, tql, state):
+    """Same metric through the public API with host buffers: per call, H2D of
+    x from pinned memory, exl3_linear, D2H of y into pinned memory; the step
+    ends with the result on the host."""
+    g = synthetic.GATE_DECODE
+    K, N, Ms = g["K"], g["N"], g["Ms"]
+    mats, ws = state["mats"], state["ws"]
+    hx = {M: torch.from_numpy(synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"])).pin_memory()
+          for M in Ms}
+    hy = {M: torch.empty((M, N), dtype=torch.float16).pin_memory() for M in Ms}
+    dx = {M: torch.empty((M, K), dtype=torch.float16, device="cuda") for M in Ms}
+    dy = {M: torch.empty((M, N), dtype=torch.float16, device="cuda") for M in Ms}
+    h2d = sum(hx[M].numel() * 2 for M in Ms)
+    d2h = sum(hy[M].numel() * 2 for M in Ms)
+    steps = max(20, min(args.steps // 20, 2000))
+
+    def step(i):
+        for j, M in enumerate(Ms):
+            dx[M].copy_(hx[M], non_blocking=True)
+            call_linear(tql, dx[M], M, mats[(i * len(Ms) + j) % len(mats)], dy[M], 128, ws, tql.EXL3_F16)
+            hy[M].copy_(dy[M], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(10):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(state["weights_per_step_bytes"] / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4),
+            "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# extras: prefill, crossover, logits
+# ---------------------------------------------------------------------------
+
+def bench_prefill(args, torch, tql, peaks):
+    K, N, bits, M = 5120, 17408, 4, 2048
+    mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
+    x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = make_ws(torch, tql, M, K, N, bits, 128)
+    iters = 5 if args.quick else 20
+    t_call = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 128, ws, tql.EXL3_F16), iters, 3)
+    xr = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    t_had = time_fn(torch, lambda: tql.exl3_hadamard128(x, xr, mat.su), iters, 2)
+    wt = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    t_rec = time_fn(torch, lambda: tql.exl3_reconstruct(mat.trellis, bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK),
+                    iters, 2)
+    flops = 2.0 * M * K * N
+    tflops = flops / (t_call * 1e-3) / 1e12
+    t_gemm = max(t_call - t_had - t_rec, 1e-6)
+    peak = peaks["bf16_tflops"]  # fp16 and bf16 share the tensor-core rate
+    return {"geometry": "K=5120 N=17408 bits=4 M=2048", "ms_per_call": round(t_call, 4),
+            "tflops": round(tflops, 1), "peak_tflops": peak, "frac": round(tflops / peak, 4),
+            "peak_kind": f"of {peaks['source']} (cuBLAS bf16 burst; fp16 same rate)",
+            "split_ms": {"hadamard": round(t_had, 4), "reconstruct": round(t_rec, 4), "gemm": round(t_gemm, 4)},
+            "gemm_tflops": round(flops / (t_gemm * 1e-3) / 1e12, 1),
+            "reconstruct_gbs": round((mat.nbytes + N * K * 2) / (t_rec * 1e-3) / 1e9, 1)}
+
+
+def bench_crossover(args, torch, tql):
+    out = {}
+    Ms = (64, 128, 256, 1024) if args.quick else synthetic.PREFILL_MS
+    for gm in synthetic.PREFILL_GEOMS:
+        K, N, bits = gm["K"], gm["N"], 4
+        mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
+        ws = make_ws(torch, tql, max(Ms), K, N, bits, 1)
+        rows = []
+        mx = None
+        for M in Ms:
+            x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
+            y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+            it = 3 if M >= 1024 else 8
+            td = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 0, ws, tql.EXL3_F16), it, 1)
+            tp = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 1, ws, tql.EXL3_F16), it, 1)
+            rows.append({"M": M, "decode_ms": round(td, 4), "prefill_ms": round(tp, 4)})
+            if mx is None and tp < td:
+                mx = M
+        out[gm["name"]] = {"rows": rows, "crossover_M": mx}
+        del ws, mat
+    return out
+
+
+def bench_logits(args, torch, tql, peaks):
+    c = synthetic.LOGITS
+    K, ns, ng, nd, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
+    mat = DevMatrix(torch, synthetic.make_matrix(K, ns, bits, seed=c["seed"]), n_gemm=ng)
+    res = {}
+    Ms = (1, 16) if args.quick else c["Ms"]
+    ws = make_ws(torch, tql, max(Ms), K, ng, bits, 128)
+    wbytes = K * ng * bits // 8
+    for M in Ms:
+        x = _dev(torch, synthetic.make_activations(M, K, seed=c["seed"]))
+        lg = torch.empty((M, ng), dtype=torch.float32, device="cuda")
+        am = torch.empty((M,), dtype=torch.int32, device="cuda")
+        fn = lambda: tql.exl3_logits_masked(x, M, K, mat.trellis, bits, ns, ng, nd, mat.su, mat.sv, lg, am, 128, ws)
+        t = time_fn(torch, fn, 3 if M >= 2048 else 10, 1)
+        r = {"ms": round(t, 4), "path": "prefill" if M >= 128 else "decode"}
+        if M >= 128:
+            r["tflops"] = round(2.0 * M * K * ng / (t * 1e-3) / 1e12, 1)
+        else:
+            r["weight_gbs"] = round(wbytes / (t * 1e-3) / 1e9, 1)
+            r["frac_hbm"] = round(r["weight_gbs"] / peaks["hbm_gbs"], 4)
+        res[str(M)] = r
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: baseline leg and reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample(budget_s: float):
+    """Times the oracle on a column sample of the decode workload (M=16
+    rows, full K), doubling the sample until one call takes >= budget_s."""
+    import oracle
+    oracle.build()
+    g = synthetic.GATE_DECODE
+    K, N, bits = g["K"], g["N"], g["bits"]
+    mat = synthetic.make_matrix(K, N, bits, seed=g["seed"])
+    x = synthetic.make_activations(16, K, seed=g["seed"], x_scale=g["x_scale"])
+    cols = 256
+    while True:
+        t0 = time.perf_counter()
+        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or cols >= N:
+            break
+        cols = min(N, cols * 2)
+    bytes_ = K * cols * bits // 8
+    return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"one M=16 call over columns [0, {cols}) of K=5120 N=17408 bits=4 "
+                      f"({bytes_} trellis bytes), {dt:.2f} s", "cols": cols, "seconds": dt}
+
+
+def run_reference(args, dist):
+    world, rank, _ = dist
+    if rank != 0:
+        return
+    import oracle
+    base = oracle_sample(0.5)
+    cols = base["cols"]
+    g = synthetic.GATE_DECODE
+    K, N, bits = g["K"], g["N"], g["bits"]
+    mat = synthetic.make_matrix(K, N, bits, seed=g["seed"])
+    x = synthetic.make_activations(16, K, seed=g["seed"], x_scale=g["x_scale"])
+    steps = max(1, min(args.steps, 20))
+    warm = max(0, min(args.warmup, 3))
+    for _ in range(warm):
+        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+    dt = (time.perf_counter() - t0) / steps
+    bytes_ = K * cols * bits // 8
+    v = bytes_ / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": synthetic.GATE_DECODE["name"], "sample_cols": cols, "rows": 16},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"each step one M=16 call over columns [0, {cols}) (full K)"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    dist = dist_info()
+    world, rank, local = dist
+    if args.impl == "reference":
+        run_reference(args, dist)
+        return
+    import torch
+    import trellis_quantized_linear_gb300 as tql
+    if world > 1:
+        torch.distributed.init_process_group(backend="nccl")
+    torch.cuda.set_device(local)
+    tql.build()
+    tql.exl3_init(local)
+    peaks = load_peaks()
+
+    dec = bench_decode(args, torch, tql, peaks, dist)
+    e2e = bench_e2e(args, torch, tql, dec)
+    extras = {}
+    if not args.no_extras and rank == 0:
+        for name, fn in (("prefill", lambda: bench_prefill(args, torch, tql, peaks)),
+                         ("crossover", lambda: bench_crossover(args, torch, tql)),
+                         ("logits", lambda: bench_logits(args, torch, tql, peaks))):
+            try:
+                extras[name] = fn()
+            except Exception as ex:  # report, never hide
+                extras[name] = {"error": repr(ex)}
+            torch.cuda.empty_cache()
+    status = tql.exl3_get_device_status()
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = oracle_sample(1.0)
+        cpu = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cpu.items() if k not in ("cols", "seconds")}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(dec["value"], 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": synthetic.GATE_DECODE["name"], "step": "exl3_linear at M=1,4,8,16 (fp16 out)",
+                       "l2": f"inputs larger than L2: {WEIGHT_COPIES} rotating weight copies "
+                             f"({WEIGHT_COPIES * dec['mats'][0].nbytes / 1e6:.0f} MB)",
+                       "timing": "CUDA graph replays, CUDA events on the launching stream",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": dec["roofline"], "clocks": dec["clocks"], "e2e": e2e,
+            "gpu_launches": dec["gpu_launches"], "per_m": dec["per_m"], "cpu_baseline": cpu,
+            "device_status": status,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

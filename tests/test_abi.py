@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function include/exl3.h declares,
+reject invalid arguments before touching the device, and carry the pages'
+host-side arithmetic (logits width alignment, scratch bound).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import trellis_quantized_linear_gb300 as tql
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tql.build()
+    return tql.load()
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    return vals
+
+
+def test_header_declarations_are_exported(lib):
+    with open(os.path.join(ROOT, "include", "exl3.h")) as f:
+        text = f.read()
+    declared = set(re.findall(r"^\s*(?:exl3_status|int|int64_t|size_t|const char \*)\s*\**\s*(exl3_\w+)\s*\(",
+                              text, flags=re.M))
+    assert declared == set(tql.HEADER_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert tql.exl3_status_string(s)
+    assert tql.exl3_status_string(99) == "unknown status"
+
+
+def test_supported_bits(lib):
+    assert [b for b in range(0, 10) if tql.exl3_supported_bits(b)] == [2, 3, 4, 5, 6, 8]
+
+
+def test_logits_width_matches_page_example(lib):
+    g = _golden("logits_width.txt")
+    n = tql.exl3_aligned_logits_width(g["n_decodable"], g["n_stored"])
+    assert n == g["n_gemm"]
+    assert n % g["align"] == 0
+    assert n - g["n_decodable"] == g["n_pad"]
+    # the clamp: the aligned width never exceeds the stored rows
+    assert tql.exl3_aligned_logits_width(300, 320) == 320
+    assert tql.exl3_aligned_logits_width(0, 10) == -1
+    assert tql.exl3_aligned_logits_width(11, 10) == -1
+
+
+def test_workspace_holds_one_reconstruct_chunk_within_page_bound(lib):
+    g = _golden("scratch_bound.txt")
+    K, chunk = g["K"], g["chunk_cols"]
+    assert chunk == tql.EXL3_RECONSTRUCT_CHUNK_COLS
+    chunk_bytes = K * chunk * g["bytes_per_weight"]
+    assert chunk_bytes <= g["bound_mb"] * 1_000_000
+    # a prefill-capable workspace for a logits-width geometry holds exactly one chunk
+    n_gemm, M = 248192, 2048
+    with_prefill = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 128, 152)
+    decode_only = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 0, 152)
+    xr = M * K * 2
+    assert with_prefill - decode_only == xr + chunk_bytes
+    # narrower than one chunk: the scratch shrinks with n_gemm (rounded to 256 rows)
+    small = tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 128, 152) - \
+        tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 0, 152)
+    assert small == xr + 17408 * K * 2
+
+
+@pytest.mark.parametrize("K,N", [(5120, 17408), (17408, 5120), (5120, 248192), (512, 512), (128, 128)])
+@pytest.mark.parametrize("sms", [148, 152, 160])
+def test_decode_plan_invariants(lib, K, N, sms):
+    S, Gs = tql.exl3_decode_plan(K, N, sms)
+    KB, NB = K // 128, N // 128
+    assert 1 <= S <= KB
+    assert -(-KB // S) <= 16          # the rotated K slice fits the CTA's shared memory
+    assert S * Gs <= sms              # one CTA per SM
+    assert Gs <= NB
+
+
+def test_decode_plan_gate_geometry_uses_whole_gpu_rounds(lib):
+    # 136 n-blocks x 40 k-blocks on 152 SMs: one round of 8 warps per CTA
+    S, Gs = tql.exl3_decode_plan(5120, 17408, 152)
+    NB = 17408 // 128
+    assert -(-NB // Gs) <= 8
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    good = 1 << 20  # a 16-byte aligned fake address; never dereferenced
+    L = lib
+    # K not a multiple of 128
+    assert L.exl3_linear(good, 4, 100, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 1
+    # n_gemm > n_stored
+    assert L.exl3_linear(good, 4, 128, good, 4, 256, 384, good, good, good, 1, 0, good, 1 << 30, None) == 1
+    # bad dtype, negative threshold, negative M
+    assert L.exl3_linear(good, 4, 128, good, 4, 256, 256, good, good, good, 7, 0, good, 1 << 30, None) == 1
+    assert L.exl3_linear(good, 4, 128, good, 4, 256, 256, good, good, good, 1, -1, good, 1 << 30, None) == 1
+    assert L.exl3_linear(good, -1, 128, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 1
+    # unsupported bits
+    assert L.exl3_linear(good, 4, 128, good, 7, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 3
+    # misaligned / null pointers
+    assert L.exl3_linear(good + 2, 4, 128, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 2
+    assert L.exl3_linear(good, 4, 128, None, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 2
+    # logits: n_decodable out of range
+    assert L.exl3_logits_masked(good, 1, 128, good, 6, 256, 256, 0, good, good, good, good, 0, good,
+                                1 << 30, None) == 1
+    assert L.exl3_logits_masked(good, 1, 128, good, 6, 256, 256, 257, good, good, good, good, 0, good,
+                                1 << 30, None) == 1
+    # reconstruct: slice not 128-aligned, bad layout
+    assert L.exl3_reconstruct(good, 4, 128, 256, 64, 128, good, 0, None) == 1
+    assert L.exl3_reconstruct(good, 4, 128, 256, 0, 128, good, 2, None) == 1
+    assert L.exl3_reconstruct(good, 4, 128, 256, 128, 256, good, 0, None) == 1
+    # hadamard: cols not a multiple of 128
+    assert L.exl3_hadamard128(good, good, None, 2, 100, None) == 1
+    assert L.exl3_hadamard128(good, good + 8, None, 2, 128, None) == 2
+    # self-test limit out of range
+    assert L.exl3_selftest_wait_timeout(0, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.reload(tql)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "libexl3.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(ImportError):
+        mod.load()
+    importlib.reload(tql)

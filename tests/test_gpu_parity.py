@@ -1,0 +1,336 @@
+"""GPU parity: every entry point of libexl3 against the CPU oracle.
+
+Bars: bit-exact for the reconstructed weights, the input rotation and the
+pad mask / argmax; max|y - y_ref| / rms(y_ref) <= 2e-3 for the fp32 layer
+output (fp32 accumulation against the oracle's fp64); the fp16 output is the
+round-to-nearest-even of the same call's fp32 output, bit for bit.
+"""
+import numpy as np
+import pytest
+
+import synthetic
+import trellis_quantized_linear_gb300 as tql
+from gpu_util import TOL, Layer, argmax_agrees, rel_err, to_dev, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tql.build()
+    torch.cuda.set_device(0)
+    tql.exl3_init(0)
+    yield
+    assert tql.exl3_get_device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# input rotation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 640), (256, 5120)])
+@pytest.mark.parametrize("with_scale", [True, False])
+def test_hadamard128_bit_exact(oracle, rows, cols, with_scale):
+    torch = torch_mod()
+    x = synthetic.make_activations(rows, cols, seed=rows + cols)
+    su = synthetic.make_matrix(cols, 128, 4, seed=rows).su if with_scale else None
+    xd = to_dev(x)
+    yd = torch.empty_like(xd)
+    tql.exl3_hadamard128(xd, yd, to_dev(su) if su is not None else None)
+    torch.cuda.synchronize()
+    ref = oracle.input_rotation(x, su).view(np.uint16)
+    got = yd.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_hadamard128_in_place(oracle):
+    torch = torch_mod()
+    x = synthetic.make_activations(9, 384, seed=3)
+    xd = to_dev(x)
+    tql.exl3_hadamard128(xd, xd, None)
+    torch.cuda.synchronize()
+    assert np.array_equal(xd.cpu().numpy().view(np.uint16), oracle.input_rotation(x).view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# reconstruct
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+@pytest.mark.parametrize("layout", [tql.EXL3_LAYOUT_KN, tql.EXL3_LAYOUT_NK])
+@pytest.mark.parametrize("n0,n_cols", [(0, 640), (256, 256)])
+def test_reconstruct_bit_exact(oracle, bits, layout, n0, n_cols):
+    torch = torch_mod()
+    K, N = 272, 640
+    m = synthetic.make_matrix(K, N, bits, seed=bits)
+    tr = to_dev(m.trellis)
+    shape = (K, n_cols) if layout == tql.EXL3_LAYOUT_KN else (n_cols, K)
+    w = torch.full(shape, 7.0, dtype=torch.float16, device="cuda")
+    tql.exl3_reconstruct(tr, bits, K, N, n0, n_cols, w, layout)
+    torch.cuda.synchronize()
+    ref = oracle.reconstruct(m.trellis, bits, K, N, n0, n_cols).view(np.uint16)
+    got = w.cpu().numpy().view(np.uint16)
+    if layout == tql.EXL3_LAYOUT_NK:
+        got = got.T
+    assert np.array_equal(got, ref)
+
+
+def test_reconstruct_full_gate_geometry_sampled(oracle):
+    torch = torch_mod()
+    K, N, bits = 5120, 17408, 4
+    m = synthetic.make_matrix(K, N, bits, seed=1)
+    tr = to_dev(m.trellis)
+    w = torch.empty((K, N), dtype=torch.float16, device="cuda")
+    tql.exl3_reconstruct(tr, bits, K, N, 0, N, w, tql.EXL3_LAYOUT_KN)
+    wt = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    tql.exl3_reconstruct(tr, bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK)
+    torch.cuda.synchronize()
+    assert torch.equal(w.t().contiguous(), wt)
+    for c0 in (0, 8704, N - 128):
+        ref = oracle.reconstruct(m.trellis, bits, K, N, c0, 128).view(np.uint16)
+        assert np.array_equal(w[:, c0:c0 + 128].cpu().numpy().view(np.uint16), ref)
+
+
+# ---------------------------------------------------------------------------
+# linear: both paths
+# ---------------------------------------------------------------------------
+
+DECODE, PREFILL = 0, 1  # m_threshold values that force each path
+
+
+@pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (128, 256, 3), (640, 384, 6), (256, 768, 2),
+                                      (384, 256, 5), (256, 256, 8)])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 37])
+def test_linear_decode_path(oracle, K, N, bits, M):
+    m = synthetic.make_matrix(K, N, bits, seed=K + N + bits)
+    x = synthetic.make_activations(M, K, seed=M)
+    L = Layer(m)
+    y = L.linear(to_dev(x), DECODE).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
+
+
+@pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6)])
+@pytest.mark.parametrize("M", [1, 32, 130, 256])
+def test_linear_prefill_path(oracle, K, N, bits, M):
+    m = synthetic.make_matrix(K, N, bits, seed=K * 3 + N + bits)
+    x = synthetic.make_activations(M, K, seed=M + 1)
+    L = Layer(m)
+    y = L.linear(to_dev(x), PREFILL).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
+
+
+def test_tiny_workload_both_paths_and_fp16_rounding(oracle):
+    t = synthetic.TINY
+    m = synthetic.make_matrix(t["K"], t["N"], t["bits"], seed=t["seed"])
+    x = synthetic.make_activations(t["M"], t["K"], seed=t["seed"], x_scale=t["x_scale"])
+    L = Layer(m)
+    xd = to_dev(x)
+    ref = oracle.linear(x, m.trellis, t["bits"], t["K"], t["N"], m.su, m.sv)
+    for thr in (DECODE, PREFILL):
+        y32 = L.linear(xd, thr, tql.EXL3_F32).cpu().numpy()
+        y16 = L.linear(xd, thr, tql.EXL3_F16).cpu().numpy()
+        assert rel_err(y32, ref) <= TOL
+        assert np.array_equal(y16.view(np.uint16), y32.astype(np.float16).view(np.uint16))
+
+
+def test_prefill_chunks_past_32768_columns(oracle):
+    # n_gemm = 32768 + 384: two reconstruct chunks, the second narrower than a GEMM tile
+    K, N, bits, M = 128, 33152, 4, 5
+    m = synthetic.make_matrix(K, N, bits, seed=9)
+    x = synthetic.make_activations(M, K, seed=9)
+    L = Layer(m)
+    xd = to_dev(x)
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    for thr in (PREFILL, DECODE):
+        y = L.linear(xd, thr).cpu().numpy()
+        assert rel_err(y, ref) <= TOL
+
+
+def test_runtime_dispatch_uses_threshold(oracle):
+    K, N, bits = 256, 256, 4
+    m = synthetic.make_matrix(K, N, bits, seed=5)
+    L = Layer(m)
+    for M in (7, 8, 9):
+        x = synthetic.make_activations(M, K, seed=M)
+        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+        y = L.linear(to_dev(x), 8).cpu().numpy()
+        assert rel_err(y, ref) <= TOL
+
+
+def test_gemm_width_narrower_than_stored(oracle):
+    K, n_stored, n_gemm, bits, M = 256, 640, 384, 4, 20
+    m = synthetic.make_matrix(K, n_stored, bits, seed=12)
+    x = synthetic.make_activations(M, K, seed=12)
+    L = Layer(m, n_gemm=n_gemm)
+    ref = oracle.linear(x, m.trellis, bits, K, n_stored, m.su, m.sv, 0, n_gemm)
+    for thr in (DECODE, PREFILL):
+        assert rel_err(L.linear(to_dev(x), thr).cpu().numpy(), ref) <= TOL
+
+
+def test_workspace_too_small_is_rejected():
+    torch = torch_mod()
+    m = synthetic.make_matrix(256, 256, 4, seed=1)
+    L = Layer(m)
+    x = to_dev(synthetic.make_activations(64, 256, seed=1))
+    need = tql.exl3_linear_workspace_bytes(64, 256, 256, 4, 1)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    y = torch.empty((64, 256), dtype=torch.float32, device="cuda")
+    with pytest.raises(tql.Exl3Error) as e:
+        tql.exl3_linear(x, 64, 256, L.trellis, 4, 256, 256, L.su, L.sv, y, tql.EXL3_F32, 1, ws, need - 256)
+    assert e.value.status == 4
+
+
+# ---------------------------------------------------------------------------
+# logits: mask + greedy selection
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("thr", [DECODE, PREFILL])
+def test_logits_mask_and_argmax_small(oracle, thr):
+    K, n_stored, n_gemm, bits, M = 256, 640, 512, 6, 6
+    m = synthetic.make_matrix(K, n_stored, bits, seed=4)
+    x = synthetic.make_activations(M, K, seed=4)
+    raw = oracle.linear(x, m.trellis, bits, K, n_stored, m.su, m.sv, 0, n_gemm)
+    n_decodable = int(np.argmax(raw[0]))  # row 0's unmasked maximum lands in the pad
+    L = Layer(m, n_gemm=n_gemm)
+    lg, am = L.logits(to_dev(x), n_decodable, thr)
+    lg = lg.cpu().numpy()
+    am = am.cpu().numpy()
+    assert np.all(np.isneginf(lg[:, n_decodable:]))
+    assert np.all(np.isfinite(lg[:, :n_decodable]))
+    assert np.array_equal(am, np.argmax(lg, axis=1))  # the CPU argmax of the GPU's own buffer
+    ref, ref_am = oracle.logits_masked(x, m.trellis, bits, K, n_stored, n_gemm, n_decodable, m.su, m.sv)
+    fin = np.isfinite(ref)
+    assert rel_err(lg[fin], ref[fin]) <= TOL
+    rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
+    argmax_agrees(am, ref, 2 * TOL * rms)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, checked on sampled 128-column blocks
+# ---------------------------------------------------------------------------
+
+def test_decode_gate_full_size_sampled(oracle):
+    g = synthetic.GATE_DECODE
+    K, N, bits = g["K"], g["N"], g["bits"]
+    m = synthetic.make_matrix(K, N, bits, seed=g["seed"])
+    L = Layer(m)
+    blocks = (0, 67, N // 128 - 1)
+    for M in g["Ms"]:
+        x = synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"])
+        y = L.linear(to_dev(x), DECODE).cpu().numpy()
+        for b in blocks:
+            ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
+            assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, (M, b)
+
+
+@pytest.mark.parametrize("geom", [0, 1])
+def test_prefill_full_size_sampled(oracle, geom):
+    gm = synthetic.PREFILL_GEOMS[geom]
+    K, N, bits = gm["K"], gm["N"], 4
+    M = 2048 if geom == 0 else 1024
+    m = synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED)
+    x = synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED)
+    L = Layer(m)
+    y = L.linear(to_dev(x), 128).cpu().numpy()
+    for b in (0, N // 128 - 1):
+        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
+        assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, b
+
+
+@pytest.mark.parametrize("M", [1, 16, 2048])
+def test_logits_full_size(oracle, M):
+    c = synthetic.LOGITS
+    K, n_stored, n_gemm, n_dec, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
+    assert tql.exl3_aligned_logits_width(n_dec, n_stored) == n_gemm
+    m = synthetic.make_matrix(K, n_stored, bits, seed=c["seed"])
+    x = synthetic.make_activations(M, K, seed=c["seed"])
+    L = Layer(m, n_gemm=n_gemm)
+    lg, am = L.logits(to_dev(x), n_dec, 128)
+    torch = torch_mod()
+    assert bool(torch.isneginf(lg[:, n_dec:]).all())
+    assert bool(torch.isfinite(lg[:, :n_dec]).all())
+    assert torch.equal(am.long(), torch.argmax(lg, dim=1))
+    rows = slice(0, min(M, 64))
+    xs = x[rows]
+    for b in (0, n_gemm // 128 - 1):
+        ref = oracle.linear(xs, m.trellis, bits, K, n_stored, m.su, m.sv, 128 * b, 128)
+        got = lg[rows, 128 * b:128 * b + 128].cpu().numpy()
+        fin = np.arange(128 * b, 128 * b + 128) < n_dec
+        assert rel_err(got[:, fin], ref[:, fin]) <= TOL
+
+
+def test_logits_full_size_argmax_against_oracle(oracle):
+    c = synthetic.LOGITS
+    K, n_stored, n_gemm, n_dec, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
+    m = synthetic.make_matrix(K, n_stored, bits, seed=c["seed"])
+    x = synthetic.make_activations(2, K, seed=c["seed"])
+    L = Layer(m, n_gemm=n_gemm)
+    lg, am = L.logits(to_dev(x), n_dec, 0)
+    ref, ref_am = oracle.logits_masked(x, m.trellis, bits, K, n_stored, n_gemm, n_dec, m.su, m.sv)
+    fin = np.isfinite(ref)
+    lgn = lg.cpu().numpy()
+    assert rel_err(lgn[fin], ref[fin]) <= TOL
+    rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
+    argmax_agrees(am.cpu().numpy(), ref, 2 * TOL * rms)
+
+
+# ---------------------------------------------------------------------------
+# graph capture: the dispatch lives inside the call
+# ---------------------------------------------------------------------------
+
+def test_graph_capture_keeps_each_path(oracle):
+    torch = torch_mod()
+    K, N, bits, thr = 256, 512, 4, 64
+    m = synthetic.make_matrix(K, N, bits, seed=21)
+    L = Layer(m)
+    ws = L.workspace(256, thr)
+    need_decode = tql.exl3_linear_workspace_bytes(8, K, N, bits, thr)  # decode-only prefix of the workspace
+    x_small = to_dev(synthetic.make_activations(8, K, seed=22))
+    x_big = to_dev(synthetic.make_activations(256, K, seed=23))
+    y_small = torch.empty((8, N), dtype=torch.float32, device="cuda")
+    y_big = torch.empty((256, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(s):
+        for xd, yd in ((x_small, y_small), (x_big, y_big)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                tql.exl3_linear(xd, xd.shape[0], K, L.trellis, bits, N, N, L.su, L.sv, yd, tql.EXL3_F32, thr, ws)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    scratch = ws[need_decode:]
+    scratch.fill_(0x5A)
+    torch.cuda.synchronize()
+    graphs[0].replay()
+    torch.cuda.synchronize()
+    assert bool((scratch == 0x5A).all()), "the decode-shaped graph touched the prefill scratch"
+    graphs[1].replay()
+    torch.cuda.synchronize()
+    assert not bool((scratch == 0x5A).all()), "the prefill-shaped graph did not use its scratch"
+    ref_s = oracle.linear(x_small.cpu().numpy(), m.trellis, bits, K, N, m.su, m.sv)
+    ref_b = oracle.linear(x_big.cpu().numpy(), m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y_small.cpu().numpy(), ref_s) <= TOL
+    assert rel_err(y_big.cpu().numpy(), ref_b) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# failure detection without a fault: a bounded wait that runs out
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_context_survives(oracle):
+    torch = torch_mod()
+    assert tql.exl3_get_device_status() == 0
+    tql.exl3_selftest_wait_timeout(2000)  # 2 ms
+    assert tql.exl3_get_device_status() == 7
+    assert tql.exl3_get_device_status() == 0  # read-and-clear
+    # the context still works
+    m = synthetic.make_matrix(128, 128, 4, seed=2)
+    x = synthetic.make_activations(3, 128, seed=2)
+    y = Layer(m).linear(to_dev(x), DECODE).cpu().numpy()
+    assert rel_err(y, oracle.linear(x, m.trellis, 4, 128, 128, m.su, m.sv)) <= TOL
+    torch.cuda.synchronize()

@@ -1,0 +1,311 @@
+// C ABI of libexl3: argument validation, workspace layout and the runtime
+// decode / prefill dispatch. Declarations and argument contracts are in
+// include/exl3.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/exl3.h"
+#include "exl3_common.cuh"
+#include "exl3_internal.h"
+
+// Device error word: kernels set it when they give up a bounded wait.
+__device__ int g_exl3_status_word;
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+const DeviceInfo *current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+  const DeviceInfo *info = &g_devices[d];
+  return info->ready ? info : nullptr;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_ok(int64_t K, int64_t n_stored, int64_t n_gemm) {
+  return K > 0 && K % 128 == 0 && K <= 131072 && n_gemm > 0 && n_gemm % 128 == 0 && n_stored % 128 == 0 &&
+         n_gemm <= n_stored;
+}
+
+exl3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA; }
+
+// Shared by exl3_linear and exl3_logits_masked once arguments are validated.
+exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const void *x, int64_t M, int64_t K,
+                       const uint16_t *trellis, int bits, int64_t n_stored, int64_t n_gemm, int64_t n_valid,
+                       const void *su, const void *sv, void *y, int y_dtype, int64_t m_threshold,
+                       uint8_t *ws, cudaStream_t st) {
+  const bool prefill = m_threshold > 0 && M >= m_threshold;
+  const size_t ysz = y_dtype == EXL3_F32 ? 4 : 2;
+  if (!prefill) {
+    for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
+      DecodeLaunch d;
+      d.x = static_cast<const uint8_t *>(x) + (size_t)(m0 * K) * 2;
+      d.rows = (int)((M - m0) < kDecodeRows ? (M - m0) : kDecodeRows);
+      d.K = K;
+      d.trellis = trellis;
+      d.bits = bits;
+      d.n_stored = n_stored;
+      d.n_gemm = n_gemm;
+      d.n_valid = n_valid;
+      d.su = su;
+      d.sv = sv;
+      d.y = static_cast<uint8_t *>(y) + (size_t)(m0 * n_gemm) * ysz;
+      d.y_f32 = y_dtype == EXL3_F32;
+      d.partials = reinterpret_cast<float *>(ws + L.partials_off);
+      d.counters = reinterpret_cast<int *>(ws + L.counters_off);
+      d.status = dev->status;
+      d.plan = L.plan;
+      cudaError_t e = launch_decode_gemm(d, st);
+      if (e != cudaSuccess) return EXL3_ERR_CUDA;
+    }
+    return EXL3_OK;
+  }
+  void *xr = ws + L.xr_off;
+  void *wchunk = ws + L.wchunk_off;
+  cudaError_t e = launch_hadamard128(x, xr, su, M, K, dev->num_sms, st);
+  if (e != cudaSuccess) return EXL3_ERR_CUDA;
+  for (int64_t c0 = 0; c0 < n_gemm; c0 += EXL3_RECONSTRUCT_CHUNK_COLS) {
+    const int64_t nc = (n_gemm - c0) < EXL3_RECONSTRUCT_CHUNK_COLS ? (n_gemm - c0) : EXL3_RECONSTRUCT_CHUNK_COLS;
+    e = launch_reconstruct(trellis, bits, K, n_stored, c0, nc, wchunk, EXL3_LAYOUT_NK, dev->num_sms, st);
+    if (e != cudaSuccess) return EXL3_ERR_CUDA;
+    PrefillLaunch p;
+    p.xr = xr;
+    p.xr_rows = L.xr_rows;
+    p.M = M;
+    p.K = K;
+    p.wt = wchunk;
+    p.chunk_rows = L.chunk_rows;
+    p.nc = nc;
+    p.sv = static_cast<const uint8_t *>(sv) + (size_t)c0 * 2;
+    p.y = static_cast<uint8_t *>(y) + (size_t)c0 * ysz;
+    p.ldy = n_gemm;
+    p.y_f32 = y_dtype == EXL3_F32;
+    p.n_valid_local = n_valid - c0;
+    p.status = dev->status;
+    p.num_sms = dev->num_sms;
+    e = launch_prefill_gemm(p, st);
+    if (e != cudaSuccess) return EXL3_ERR_CUDA;
+  }
+  return EXL3_OK;
+}
+
+// Validation shared by exl3_linear and exl3_logits_masked. On success fills
+// `layout` for this call's M.
+exl3_status validate_linear(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits,
+                            int64_t n_stored, int64_t n_gemm, const void *su, const void *sv, const void *y,
+                            int64_t m_threshold, void *workspace, size_t workspace_bytes,
+                            const DeviceInfo **dev_out, WorkspaceLayout *layout) {
+  if (M < 0 || M > (int64_t)1 << 31 || m_threshold < 0 || !shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
+  if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
+  if (!aligned16(x) || !aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(y) ||
+      !aligned16(workspace))
+    return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  if (!workspace_layout(M, K, n_gemm, bits, m_threshold, dev->num_sms, layout)) return EXL3_ERR_INVALID_ARG;
+  if (layout->total > workspace_bytes) return EXL3_ERR_WORKSPACE_TOO_SMALL;
+  *dev_out = dev;
+  return EXL3_OK;
+}
+
+}  // namespace
+
+bool bits_supported(int bits) {
+  return bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8;
+}
+
+bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold, int num_sms,
+                      WorkspaceLayout *out) {
+  if (M_max < 0 || m_threshold < 0 || num_sms <= 0 || !bits_supported(bits)) return false;
+  if (K <= 0 || K % 128 || K > 131072 || n_gemm <= 0 || n_gemm % 128) return false;
+  WorkspaceLayout L;
+  const int64_t NB = n_gemm / 128, KB = K / 128;
+  L.plan = decode_plan(NB, KB, num_sms);
+  size_t off = 0;
+  L.counters_off = off;
+  off += align_up((size_t)NB * 4, 256);
+  L.partials_off = off;
+  if (L.plan.S > 1) off += align_up((size_t)L.plan.S * kDecodeRows * (size_t)n_gemm * 4, 256);
+  L.prefill = m_threshold > 0 && M_max >= m_threshold;
+  if (L.prefill) {
+    L.xr_rows = ceil_div(M_max, 128) * 128;
+    L.xr_off = off;
+    off += align_up((size_t)L.xr_rows * (size_t)K * 2, 256);
+    const int64_t cols = n_gemm < EXL3_RECONSTRUCT_CHUNK_COLS ? n_gemm : EXL3_RECONSTRUCT_CHUNK_COLS;
+    L.chunk_rows = ceil_div(cols, 256) * 256;
+    L.wchunk_off = off;
+    off += align_up((size_t)L.chunk_rows * (size_t)K * 2, 256);
+  }
+  L.total = off;
+  *out = L;
+  return true;
+}
+
+}  // namespace exl3
+
+using namespace exl3;
+
+extern "C" {
+
+exl3_status exl3_init(int device) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (device < 0 || device >= n || device >= kMaxDevices) return EXL3_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (cudaSetDevice(device) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (g_devices[device].ready) return EXL3_OK;
+  DeviceInfo info;
+  if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  void *status = nullptr;
+  if (cudaGetSymbolAddress(&status, g_exl3_status_word) != cudaSuccess) return EXL3_ERR_CUDA;
+  info.status = static_cast<int *>(status);
+  if (cudaMemset(info.status, 0, sizeof(int)) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (init_rotate_kernels() != cudaSuccess || init_reconstruct_kernels() != cudaSuccess ||
+      init_decode_kernels() != cudaSuccess || init_prefill_kernels() != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return EXL3_ERR_CUDA;
+  info.ready = true;
+  g_devices[device] = info;
+  return EXL3_OK;
+}
+
+const char *exl3_status_string(int status) {
+  switch (status) {
+    case EXL3_OK: return "ok";
+    case EXL3_ERR_INVALID_ARG: return "invalid argument (shape, size or enum out of range)";
+    case EXL3_ERR_ALIGNMENT: return "pointer is NULL or not 16-byte aligned";
+    case EXL3_ERR_UNSUPPORTED_BITS: return "unsupported trellis bit width";
+    case EXL3_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than the required size";
+    case EXL3_ERR_NOT_INITIALIZED: return "exl3_init was not called for the current device";
+    case EXL3_ERR_CUDA: return "CUDA runtime error or failed launch";
+    case EXL3_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
+    default: return "unknown status";
+  }
+}
+
+int exl3_supported_bits(int bits) { return bits_supported(bits) ? 1 : 0; }
+
+int64_t exl3_aligned_logits_width(int64_t n_decodable, int64_t n_stored) {
+  if (n_decodable <= 0 || n_stored <= 0 || n_decodable > n_stored) return -1;
+  const int64_t aligned = ceil_div(n_decodable, 128) * 128;
+  return aligned < n_stored ? aligned : n_stored;
+}
+
+int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *ctas_per_split) {
+  if (K <= 0 || K % 128 || K > 131072 || n_gemm <= 0 || n_gemm % 128 || num_sms <= 0 || !splits ||
+      !ctas_per_split)
+    return -1;
+  DecodePlan p = decode_plan(n_gemm / 128, K / 128, num_sms);
+  *splits = p.S;
+  *ctas_per_split = p.Gs;
+  return 0;
+}
+
+size_t exl3_linear_workspace_bytes_for(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold,
+                                       int num_sms) {
+  WorkspaceLayout L;
+  if (!workspace_layout(M_max, K, n_gemm, bits, m_threshold, num_sms, &L)) return 0;
+  return L.total;
+}
+
+size_t exl3_linear_workspace_bytes(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold) {
+  int d = -1, sms = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return 0;
+  if (d >= 0 && d < kMaxDevices && g_devices[d].ready) {
+    sms = g_devices[d].num_sms;
+  } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+    return 0;
+  }
+  return exl3_linear_workspace_bytes_for(M_max, K, n_gemm, bits, m_threshold, sms);
+}
+
+exl3_status exl3_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGNMENT;
+  if (!current_device()) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+exl3_status exl3_hadamard128(const void *x, void *y, const void *pre_scale, int64_t rows, int64_t cols,
+                             void *stream) {
+  if (rows < 0 || cols <= 0 || cols % 128) return EXL3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (pre_scale && !aligned16(pre_scale))) return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(launch_hadamard128(x, y, pre_scale, rows, cols, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+exl3_status exl3_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored, int64_t n0,
+                             int64_t n_cols, void *w, int layout, void *stream) {
+  if (K <= 0 || K % 16 || n_stored <= 0 || n_stored % 128 || n0 < 0 || n0 % 128 || n_cols < 0 || n_cols % 128 ||
+      n0 + n_cols > n_stored || (layout != EXL3_LAYOUT_KN && layout != EXL3_LAYOUT_NK))
+    return EXL3_ERR_INVALID_ARG;
+  if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
+  if (!aligned16(trellis) || !aligned16(w)) return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(launch_reconstruct(trellis, bits, K, n_stored, n0, n_cols, w, layout, dev->num_sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+exl3_status exl3_linear(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits, int64_t n_stored,
+                        int64_t n_gemm, const void *su, const void *sv, void *y, int y_dtype, int64_t m_threshold,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+  if (y_dtype != EXL3_F16 && y_dtype != EXL3_F32) return EXL3_ERR_INVALID_ARG;
+  const DeviceInfo *dev = nullptr;
+  WorkspaceLayout L;
+  exl3_status s = validate_linear(x, M, K, trellis, bits, n_stored, n_gemm, su, sv, y, m_threshold, workspace,
+                                  workspace_bytes, &dev, &L);
+  if (s != EXL3_OK) return s;
+  if (M == 0) return EXL3_OK;
+  return run_linear(dev, L, x, M, K, trellis, bits, n_stored, n_gemm, n_gemm, su, sv, y, y_dtype, m_threshold,
+                    static_cast<uint8_t *>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+exl3_status exl3_logits_masked(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits,
+                               int64_t n_stored, int64_t n_gemm, int64_t n_decodable, const void *su,
+                               const void *sv, float *logits, int32_t *argmax, int64_t m_threshold,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  if (n_decodable < 1 || n_decodable > n_gemm) return EXL3_ERR_INVALID_ARG;
+  const DeviceInfo *dev = nullptr;
+  WorkspaceLayout L;
+  exl3_status s = validate_linear(x, M, K, trellis, bits, n_stored, n_gemm, su, sv, logits, m_threshold,
+                                  workspace, workspace_bytes, &dev, &L);
+  if (s != EXL3_OK) return s;
+  if (!aligned16(argmax)) return EXL3_ERR_ALIGNMENT;
+  if (M == 0) return EXL3_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = run_linear(dev, L, x, M, K, trellis, bits, n_stored, n_gemm, n_decodable, su, sv, logits, EXL3_F32,
+                 m_threshold, static_cast<uint8_t *>(workspace), st);
+  if (s != EXL3_OK) return s;
+  return from_cuda(launch_argmax(logits, M, n_gemm, argmax, st));
+}
+
+exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return EXL3_ERR_INVALID_ARG;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(launch_wait_timeout_selftest(dev->status, (unsigned long long)limit_us * 1000ull,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+exl3_status exl3_get_device_status(void *stream) {
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXL3_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (v != 0 && cudaMemset(dev->status, 0, sizeof(int)) != cudaSuccess) return EXL3_ERR_CUDA;
+  return v == 0 ? EXL3_OK : static_cast<exl3_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Host-side interfaces between the libexl3 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace exl3 {
+
+constexpr int kDecodeConsumerWarps = 8;   // consumer warps per decode-GEMM CTA
+constexpr int kDecodeMaxKSplit = 2048;    // largest K range one decode CTA rotates into smem
+constexpr int kDecodeRows = 16;           // activation rows per decode-GEMM launch
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Split-K / n-block assignment of the decode-shaped GEMM.
+struct DecodePlan {
+  int S = 1;   // K splits (each a whole number of 128-row blocks)
+  int Gs = 1;  // CTAs per split; CTA (ks, gs) owns n-blocks gs, gs+Gs, ...
+  int grid() const { return S * Gs; }
+};
+DecodePlan decode_plan(int64_t n_blocks, int64_t k_blocks, int num_sms);
+
+// Workspace layout shared by the size query and the calls.
+struct WorkspaceLayout {
+  DecodePlan plan;
+  size_t counters_off = 0, partials_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
+  int64_t xr_rows = 0;      // rows of the rotated-activation buffer (multiple of 128)
+  int64_t chunk_rows = 0;   // rows of the reconstruct chunk (multiple of 256)
+  bool prefill = false;
+};
+bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold,
+                      int num_sms, WorkspaceLayout *out);
+
+struct DecodeLaunch {
+  const void *x;          // rows m0.. of x (fp16), ld = K
+  int rows;               // 1..16
+  int64_t K;
+  const uint16_t *trellis;
+  int bits;
+  int64_t n_stored, n_gemm, n_valid;
+  const void *su, *sv;
+  void *y;                // rows m0.. of y, ld = n_gemm
+  int y_f32;
+  float *partials;        // S x 16 x n_gemm fp32 (unused when S == 1)
+  int *counters;          // n_gemm/128 int32, zero between calls
+  int *status;
+  DecodePlan plan;
+};
+
+struct PrefillLaunch {
+  const void *xr;         // rotated activations, xr_rows x K fp16
+  int64_t xr_rows, M, K;
+  const void *wt;         // reconstructed chunk, W^T, chunk_rows x K fp16
+  int64_t chunk_rows, nc; // rows allocated / columns used (nc % 128 == 0)
+  const void *sv;         // sv + c0
+  void *y;                // y + c0 (element offset), ld = ldy
+  int64_t ldy;
+  int y_f32;
+  int64_t n_valid_local;  // columns >= this are written as -inf
+  int *status;
+  int num_sms;
+};
+
+cudaError_t init_rotate_kernels();
+cudaError_t init_reconstruct_kernels();
+cudaError_t init_decode_kernels();
+cudaError_t init_prefill_kernels();
+
+cudaError_t launch_hadamard128(const void *x, void *y, const void *pre, int64_t rows, int64_t cols,
+                               int num_sms, cudaStream_t st);
+cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored,
+                               int64_t n0, int64_t n_cols, void *w, int layout, int num_sms,
+                               cudaStream_t st);
+cudaError_t launch_decode_gemm(const DecodeLaunch &p, cudaStream_t st);
+cudaError_t launch_prefill_gemm(const PrefillLaunch &p, cudaStream_t st);
+cudaError_t launch_argmax(const float *logits, int64_t M, int64_t n, int32_t *argmax,
+                          cudaStream_t st);
+
+bool bits_supported(int bits);
+cudaError_t launch_wait_timeout_selftest(int *status, unsigned long long limit_ns, cudaStream_t st);
+
+}  // namespace exl3

@@ -1,0 +1,361 @@
+// Prefill-shaped dense GEMM on the 5th-generation tensor cores (tcgen05),
+// with the output rotation fused into its epilogue:
+//
+//     y[:, c0:c0+nc] = had_r_128( x' . W[:, c0:c0+nc] ) * sv[c0:c0+nc]
+//
+// This is the "hgemm" stage of the unfused prefill sequence of vLLM PR #316,
+// "[EXL3] dispatch prefill-shaped GEMMs to reconstruct+hgemm" (sections
+// "Kernel measurements" and "Change"), rebuilt for sm_103a, plus the final
+// had_r_128 of that sequence.
+//
+// A = x' (rotated activations, rows x K fp16, K-major) and B = W^T (the
+// reconstructed chunk, nc x K fp16, K-major) are staged by TMA with 128-byte
+// swizzle into a 4-stage ring; one thread issues tcgen05.mma (M=128, N=256,
+// K=16, fp32 accumulation in TMEM); the accumulator is double-buffered in
+// TMEM (2 x 256 columns) so the epilogue of tile i overlaps the main loop of
+// tile i+1. Persistent grid, one CTA per SM.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator
+// and MMA issuer, warps 2..5 = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, i.e. one output row per thread).
+//
+// Roofline: tensor-bound, 2*M*K*nc flops per launch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "exl3_common.cuh"
+#include "exl3_internal.h"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + 256;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand with 128-byte
+// swizzle: start address >> 4 (bits 0-13), leading byte offset (unused for
+// this layout, encoded 1), stride byte offset 1024 B between 8-row groups
+// (bits 32-45), fixed version 1 at bits 46-47, swizzle mode 2 (128 B) at
+// bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+struct PrefillParams {
+  const __half *sv;
+  void *y;
+  int *status;
+  int64_t ldy, n_valid_local;
+  int M, nc, K, y_f32, tiles_m, tiles_n;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Loads 32 consecutive fp32 TMEM columns of this thread's lane and waits for
+// them inside the same asm statement, so no use can be scheduled before the
+// wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// In-register orthonormal had_r_128 of one row block, then * sv, mask, store.
+__device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillParams &p, int64_t row, int col0) {
+#pragma unroll
+  for (int h = 1; h < 128; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+      if (!(i & h)) {
+        float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+  const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
+#pragma unroll
+  for (int a = 0; a < 16; ++a) {
+    uint4 raw = __ldg(svp + a);
+    const __half *h = reinterpret_cast<const __half *>(&raw);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = 8 * a + e;
+      v[c] = (col0 + c < p.n_valid_local) ? v[c] * (__half2float(h[e]) * kInvSqrt128) : -INFINITY;
+    }
+  }
+  if (row >= p.M) return;
+  if (p.y_f32) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + row * p.ldy + col0);
+#pragma unroll
+    for (int a = 0; a < 32; ++a) dst[a] = make_float4(v[4 * a], v[4 * a + 1], v[4 * a + 2], v[4 * a + 3]);
+  } else {
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.y) + row * p.ldy + col0);
+#pragma unroll
+    for (int a = 0; a < 16; ++a) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __half2 h2 = __floats2half2_rn(v[8 * a + 2 * e], v[8 * a + 2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t *>(&h2);
+      }
+      dst[a] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  const uint32_t smem_s = smem_u32(smem);
+  auto a_s = [&](int s) { return smem_s + (uint32_t)(s * A_BYTES); };
+  auto b_s = [&](int s) { return smem_s + (uint32_t)(STAGES * A_BYTES + s * B_BYTES); };
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
+  const uint32_t done_bar = smem_u32(&bars[2 * STAGES + 4]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = p.tiles_m * p.tiles_n;
+  const int kblocks = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
+        tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
+        tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      const int64_t uses = issued / STAGES + (s < issued % STAGES ? 1 : 0);
+      if (uses > 0) mbar_wait_short(full_bar(s), (uint32_t)((uses - 1) & 1));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.status)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(a_s(stage));
+        const uint64_t bd = sw128_desc(b_s(stage));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // +32 bytes per 16-element K step inside the 128-byte swizzle atom
+          tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tfull_bar(acc));
+    }
+    // All issued MMAs must finish before TMEM is released.
+    tc_commit(done_bar);
+    mbar_wait_short(done_bar, 0);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int lg = warp & 3;  // TMEM lane group this warp may access
+    const int row_in_tile = lg * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(tfull_bar(acc), use & 1u, p.status)) break;
+      tc_fence_after();
+      const int64_t row = (int64_t)tm * BM + row_in_tile;
+      const uint32_t tbase = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * BN);
+      const int c0 = tn * BN;
+      const bool second = c0 + 128 < p.nc;
+      float v[128];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float t[32];
+        tmem_ld32(tbase + 32 * j, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
+      }
+      if (!second) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+      }
+      epilogue_block(v, p, row, c0);
+      if (second) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float t[32];
+          tmem_ld32(tbase + 128 + 32 * j, t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
+        }
+          tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        epilogue_block(v, p, row, c0 + 128);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t init_prefill_kernels() {
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
+  if (L.M == 0 || L.nc == 0) return cudaSuccess;
+  alignas(64) CUtensorMap ma, mb;
+  if (!make_map(&ma, L.xr, L.xr_rows, L.K, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, L.wt, L.chunk_rows, L.K, BN)) return cudaErrorInvalidValue;
+  PrefillParams p;
+  p.sv = static_cast<const __half *>(L.sv);
+  p.y = L.y;
+  p.status = L.status;
+  p.ldy = L.ldy;
+  p.n_valid_local = L.n_valid_local;
+  p.M = (int)L.M;
+  p.nc = (int)L.nc;
+  p.K = (int)L.K;
+  p.y_f32 = L.y_f32;
+  p.tiles_m = (int)ceil_div(L.M, BM);
+  p.tiles_n = (int)ceil_div(L.nc, BN);
+  const int ntiles = p.tiles_m * p.tiles_n;
+  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  prefill_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace exl3
