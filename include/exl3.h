@@ -64,7 +64,8 @@ typedef enum {
     EXL3_ERR_WORKSPACE_TOO_SMALL = 4,/* workspace_bytes below the required size */
     EXL3_ERR_NOT_INITIALIZED = 5,    /* exl3_init was not called for the current device */
     EXL3_ERR_CUDA = 6,               /* a CUDA runtime call or a launch failed */
-    EXL3_ERR_DEVICE_TIMEOUT = 7      /* a kernel gave up a bounded wait (see exl3_get_device_status) */
+    EXL3_ERR_DEVICE_TIMEOUT = 7,     /* a kernel gave up a bounded wait (see exl3_get_device_status) */
+    EXL3_ERR_NOALLOC_TOO_LARGE = 8   /* the problem needs more scratch than the fixed no-alloc buffer holds */
 } exl3_status;
 
 typedef enum { EXL3_F16 = 0, EXL3_F32 = 1 } exl3_dtype;
@@ -212,6 +213,32 @@ exl3_status exl3_get_device_status(void *stream);
  * counterpart; it exercises the bounded waits every pipelined kernel uses.
  */
 exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+/*
+ * exl3_linear_decode_noalloc: the decode-shaped exl3_linear (as with
+ * m_threshold == 0) for callers that cannot allocate device memory: a
+ * plugin inside a host program that owns every device buffer, or code that
+ * must not call cudaMalloc at run time because it synchronises the whole
+ * device. The caller passes only inputs and outputs; the split-K partial
+ * sums and completion counters live in a fixed 16 MiB buffer inside the
+ * library (a static device array that every GPU which loads libexl3.so
+ * keeps until the process exits). The pages have no counterpart to this
+ * entry point.
+ *   Arguments as exl3_linear, without m_threshold and workspace.
+ *   Limit: exl3_linear_workspace_bytes(16, K, n_gemm, bits, 0) must not
+ *   exceed 16 MiB (the MLP projections fit; a 248192-wide logits layer does
+ *   not); larger problems return EXL3_ERR_NOALLOC_TOO_LARGE and launch
+ *   nothing.
+ *   The first call on a device looks up the buffer's device address, so
+ *   make that first call before any stream capture. Each call clears the
+ *   counters it needs on `stream` first. Every call shares the one buffer
+ *   and it keeps the last call's contents, so calls that may overlap on the
+ *   GPU (different streams, no ordering) race: order them. It never calls
+ *   cudaMalloc, cudaFree or any allocating routine. exl3_init must have run.
+ */
+exl3_status exl3_linear_decode_noalloc(const void *x, int64_t M, int64_t K, const uint16_t *trellis,
+                                       int bits, int64_t n_stored, int64_t n_gemm, const void *su,
+                                       const void *sv, void *y, int y_dtype, void *stream);
 
 #ifdef __cplusplus
 }

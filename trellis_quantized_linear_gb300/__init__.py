@@ -18,7 +18,7 @@ __all__ = [
     "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_linear_workspace_bytes_for",
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
-    "HEADER_SYMBOLS",
+    "exl3_linear_decode_noalloc", "HEADER_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,7 @@ EXL3_RECONSTRUCT_CHUNK_COLS = 32768
 STATUS_NAMES = {
     0: "EXL3_OK", 1: "EXL3_ERR_INVALID_ARG", 2: "EXL3_ERR_ALIGNMENT", 3: "EXL3_ERR_UNSUPPORTED_BITS",
     4: "EXL3_ERR_WORKSPACE_TOO_SMALL", 5: "EXL3_ERR_NOT_INITIALIZED", 6: "EXL3_ERR_CUDA",
-    7: "EXL3_ERR_DEVICE_TIMEOUT",
+    7: "EXL3_ERR_DEVICE_TIMEOUT", 8: "EXL3_ERR_NOALLOC_TOO_LARGE",
 }
 
 # Every function include/exl3.h declares.
@@ -42,6 +42,7 @@ HEADER_SYMBOLS = (
     "exl3_decode_plan", "exl3_linear_workspace_bytes_for", "exl3_linear_workspace_bytes",
     "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct", "exl3_linear",
     "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
+    "exl3_linear_decode_noalloc",
 )
 
 
@@ -91,6 +92,8 @@ def load():
                                                   _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp]),
             "exl3_get_device_status": (ctypes.c_int, [_vp]),
             "exl3_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _vp]),
+            "exl3_linear_decode_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i64, _vp, _vp,
+                                                          _vp, ctypes.c_int, _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -207,3 +210,12 @@ def exl3_get_device_status(stream=None) -> int:
 def exl3_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Launches the bounded-wait self-test kernel (see include/exl3.h)."""
     _check(load().exl3_selftest_wait_timeout(int(limit_us), _stream(stream)), "exl3_selftest_wait_timeout")
+
+
+def exl3_linear_decode_noalloc(x, M: int, K: int, trellis, bits: int, n_stored: int, n_gemm: int, su, sv, y,
+                               y_dtype: int, stream=None) -> None:
+    """Decode-shaped linear layer that allocates nothing: its scratch is a
+    fixed 16 MiB buffer inside the library (see include/exl3.h)."""
+    _check(load().exl3_linear_decode_noalloc(_ptr(x), int(M), int(K), _ptr(trellis), int(bits), int(n_stored),
+                                             int(n_gemm), _ptr(su), _ptr(sv), _ptr(y), int(y_dtype),
+                                             _stream(stream)), "exl3_linear_decode_noalloc")

@@ -119,6 +119,8 @@ exl3_status validate_linear(const void *x, int64_t M, int64_t K, const uint16_t 
 
 }  // namespace
 
+const DeviceInfo *initialized_device() { return current_device(); }
+
 bool bits_supported(int bits) {
   return bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8;
 }
@@ -189,6 +191,7 @@ const char *exl3_status_string(int status) {
     case EXL3_ERR_NOT_INITIALIZED: return "exl3_init was not called for the current device";
     case EXL3_ERR_CUDA: return "CUDA runtime error or failed launch";
     case EXL3_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
+    case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed 16 MiB no-alloc buffer";
     default: return "unknown status";
   }
 }

@@ -79,6 +79,10 @@ cudaError_t launch_argmax(const float *logits, int64_t M, int64_t n, int32_t *ar
                           cudaStream_t st);
 
 bool bits_supported(int bits);
+
+struct DeviceInfo;
+// The current device's cached set-up, or nullptr before exl3_init.
+const DeviceInfo *initialized_device();
 cudaError_t launch_wait_timeout_selftest(int *status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace exl3
