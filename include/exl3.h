@@ -104,15 +104,18 @@ int64_t exl3_aligned_logits_width(int64_t n_decodable, int64_t n_stored);
 
 /*
  * The decode-shaped path's work split for a (K, n_gemm) geometry on a GPU
- * with `num_sms` SMs: *splits K ranges (split-K factor) times
- * *ctas_per_split CTAs. Returns 0, or -1 on invalid input. Host only.
+ * with `num_sms` SMs, for calls of at most 8 rows: the whole (128-column
+ * n-block x 16-row k slab) space is cut into equal contiguous ranges, one
+ * per warp (stream-K); *splits receives the largest number of warps that
+ * share one n-block (its partial-sum slots) and *ctas_per_split the number
+ * of CTAs launched. Returns 0, or -1 on invalid input. Host only.
  */
 int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *ctas_per_split);
 
 /*
  * Workspace bytes an exl3_linear / exl3_logits_masked call with M <= M_max
  * needs on a GPU with `num_sms` streaming multiprocessors. The workspace is
- * laid out as: decode-path completion counters and split-K partial sums;
+ * laid out as: decode-path split-K partial sums and rotated activations;
  * then, when a prefill-shaped call is possible (m_threshold > 0 and
  * M_max >= m_threshold), the rotated activations (M_max x K fp16) and one
  * reconstruct chunk (min(n_gemm, 32768) x K fp16) ([P1] "Change": one
@@ -127,9 +130,9 @@ size_t exl3_linear_workspace_bytes(int64_t M_max, int64_t K, int64_t n_gemm, int
                                    int64_t m_threshold);
 
 /*
- * Clears a workspace (cudaMemsetAsync on `stream`). Call once after
- * allocating it; the library keeps the counters it holds at zero after
- * every completed call.
+ * Clears a workspace (cudaMemsetAsync on `stream`). Optional: no call needs
+ * particular initial workspace contents; it only makes a fresh buffer's
+ * contents defined.
  */
 exl3_status exl3_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
@@ -220,7 +223,7 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
  * plugin inside a host program that owns every device buffer, or code that
  * must not call cudaMalloc at run time because it synchronises the whole
  * device. The caller passes only inputs and outputs; the split-K partial
- * sums and completion counters live in a fixed 16 MiB buffer inside the
+ * sums and rotated activations live in a fixed 16 MiB buffer inside the
  * library (a static device array that every GPU which loads libexl3.so
  * keeps until the process exits). The pages have no counterpart to this
  * entry point.
@@ -230,8 +233,8 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
  *   not); larger problems return EXL3_ERR_NOALLOC_TOO_LARGE and launch
  *   nothing.
  *   The first call on a device looks up the buffer's device address, so
- *   make that first call before any stream capture. Each call clears the
- *   counters it needs on `stream` first. Every call shares the one buffer
+ *   make that first call before any stream capture. No call needs the
+ *   buffer to start at zero. Every call shares the one buffer
  *   and it keeps the last call's contents, so calls that may overlap on the
  *   GPU (different streams, no ordering) race: order them. It never calls
  *   cudaMalloc, cudaFree or any allocating routine. exl3_init must have run.

@@ -44,7 +44,7 @@ def test_header_declarations_are_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(8):
+    for s in range(9):
         assert tql.exl3_status_string(s)
     assert tql.exl3_status_string(99) == "unknown status"
 
@@ -83,22 +83,37 @@ def test_workspace_holds_one_reconstruct_chunk_within_page_bound(lib):
     assert small == xr + 17408 * K * 2
 
 
+def _owner(z, P, TS):
+    return ((z + 1) * P - 1) // TS
+
+
 @pytest.mark.parametrize("K,N", [(5120, 17408), (17408, 5120), (5120, 248192), (512, 512), (128, 128)])
 @pytest.mark.parametrize("sms", [148, 152, 160])
 def test_decode_plan_invariants(lib, K, N, sms):
-    S, Gs = tql.exl3_decode_plan(K, N, sms)
-    KB, NB = K // 128, N // 128
-    assert 1 <= S <= KB
-    assert -(-KB // S) <= 16          # the rotated K slice fits the CTA's shared memory
-    assert S * Gs <= sms              # one CTA per SM
-    assert Gs <= NB
+    """Stream-K split: 16 warps per CTA, one CTA per SM, every warp at least
+    one slab; slots = the most warps sharing one 128-column n-block."""
+    slots, ctas = tql.exl3_decode_plan(K, N, sms)
+    KT, NB = K // 16, N // 128
+    TS = NB * KT
+    P = min(16 * sms, TS)
+    assert ctas == -(-P // 16) and ctas <= sms
+    want = max(_owner((nb + 1) * KT - 1, P, TS) - _owner(nb * KT, P, TS) + 1 for nb in range(NB))
+    assert slots == want
+    # each warp owns a non-empty, contiguous range and the ranges tile the slab space
+    z = [p * TS // P for p in range(P + 1)]
+    assert z[0] == 0 and z[-1] == TS and all(b > a for a, b in zip(z, z[1:]))
 
 
-def test_decode_plan_gate_geometry_uses_whole_gpu_rounds(lib):
-    # 136 n-blocks x 40 k-blocks on 152 SMs: one round of 8 warps per CTA
-    S, Gs = tql.exl3_decode_plan(5120, 17408, 152)
-    NB = 17408 // 128
-    assert -(-NB // Gs) <= 8
+def test_decode_plan_gate_geometry_fills_every_sm(lib):
+    slots, ctas = tql.exl3_decode_plan(5120, 17408, 152)
+    assert ctas == 152 and slots == 19
+
+
+def test_noalloc_limit_covers_mlp_geometries(lib):
+    lim = 16 << 20
+    for K, N, bits in ((5120, 17408, 4), (17408, 5120, 4), (5120, 17408, 3)):
+        assert tql.exl3_linear_workspace_bytes_for(16, K, N, bits, 0, 152) <= lim
+    assert tql.exl3_linear_workspace_bytes_for(16, 5120, 248192, 6, 0, 152) > lim
 
 
 def test_invalid_arguments_are_rejected_before_any_launch(lib):

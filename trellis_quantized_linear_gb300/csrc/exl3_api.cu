@@ -60,8 +60,8 @@ exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const vo
       d.sv = sv;
       d.y = static_cast<uint8_t *>(y) + (size_t)(m0 * n_gemm) * ysz;
       d.y_f32 = y_dtype == EXL3_F32;
+      d.xf = ws + L.xf_off;
       d.partials = reinterpret_cast<float *>(ws + L.partials_off);
-      d.counters = reinterpret_cast<int *>(ws + L.counters_off);
       d.status = dev->status;
       d.plan = L.plan;
       cudaError_t e = launch_decode_gemm(d, st);
@@ -133,10 +133,10 @@ bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_
   const int64_t NB = n_gemm / 128, KB = K / 128;
   L.plan = decode_plan(NB, KB, num_sms);
   size_t off = 0;
-  L.counters_off = off;
-  off += align_up((size_t)NB * 4, 256);
   L.partials_off = off;
-  if (L.plan.S > 1) off += align_up((size_t)L.plan.S * kDecodeRows * (size_t)n_gemm * 4, 256);
+  off += align_up(decode_partials_bytes(L.plan, NB), 256);
+  L.xf_off = off;
+  off += align_up((size_t)K * 32, 256);
   L.prefill = m_threshold > 0 && M_max >= m_threshold;
   if (L.prefill) {
     L.xr_rows = ceil_div(M_max, 128) * 128;
@@ -209,8 +209,8 @@ int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *c
       !ctas_per_split)
     return -1;
   DecodePlan p = decode_plan(n_gemm / 128, K / 128, num_sms);
-  *splits = p.S;
-  *ctas_per_split = p.Gs;
+  *splits = (int)p.smax[0];
+  *ctas_per_split = (int)p.grid[0];
   return 0;
 }
 

@@ -37,8 +37,11 @@ constexpr float kInvSqrt128 = 0.0883883476483184405f;
 
 // Masked LCG word of one 16-bit state: two fp16 halves, each in +-[1/8, 2).
 __device__ __forceinline__ uint32_t lcg_word(uint32_t state) {
-  uint32_t u = state * kLcgMul + kLcgAdd;
-  return (u & kKeepMask) ^ kFlipBits;
+  const uint32_t u = state * kLcgMul + kLcgAdd;
+  uint32_t r;
+  // (u & kKeepMask) ^ kFlipBits as one three-input logic op (LUT 0x6A).
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(u), "r"(kKeepMask), "r"(kFlipBits));
+  return r;
 }
 
 // Weights of two states packed as half2 {lo: state_a, hi: state_b}.
@@ -92,6 +95,8 @@ struct RowWindows {
     constexpr int s = R * BITS * 16 + (C + 1) * BITS;  // window start, in seq bits
     constexpr int j = s >> 4;
     constexpr int o = s & 15;
+    static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
+    static_assert(o == 0 ? (j >= 1 && j <= kWords) : (j >= 0 && j < kWords), "window outside X");
     if constexpr (o == 0) {
       return X[j - 1] & 0xFFFFu;  // seq[j]
     } else if constexpr (o == 8) {

@@ -1,440 +1,609 @@
-// Decode-shaped trellis linear: one fused kernel per <= 16 activation rows.
+// Decode-shaped trellis linear: the fused decode-inside-GEMM path for up to
+// 16 activation rows per launch.
 //
-// The fused decode-inside-GEMM path of vLLM PR #316, "[EXL3] dispatch
-// prefill-shaped GEMMs to reconstruct+hgemm" (sections "Problem" and
-// "Change": the op keeps its decode-shaped kernel below the M threshold),
+// The decode-shaped kernel of vLLM PR #316, "[EXL3] dispatch prefill-shaped
+// GEMMs to reconstruct+hgemm" (sections "Problem" and "Change": below the M
+// threshold the op keeps a kernel that decodes the trellis inside the GEMM),
 // rebuilt for sm_103a. Each weight is decoded exactly once per launch.
 //
-// Structure of a CTA (1 producer warp + 8 consumer warps, 1 CTA per SM):
-//   * the CTA owns one K split [kb0, kb1) (in 128-row blocks) and the
-//     n-blocks gs, gs+Gs, ... (128 output columns each); each consumer warp
-//     owns one n-block at a time and walks the whole K split;
-//   * prologue: the consumer warps rotate their K slice of x,
-//     x' = RNE_fp16(had_r_128(x * su)), into shared memory, already laid out
-//     as mma.sync A fragments;
-//   * producer: one lane streams each warp's 16 x 128 slab of bitstreams
-//     (8 tiles, 256*BITS contiguous bytes) into a shared-memory ring with
-//     cp.async.bulk, one mbarrier pair per stage;
-//   * consumer lane (g, q) decodes tile g rows 4q..4q+3 straight into
-//     m16n8k16 B fragments: the mma's k index 2q, 2q+1, 2q+8, 2q+9 is mapped
-//     to tile rows 4q .. 4q+3 (the same permutation is applied to x'), and
-//     mma j's column g to tile column 16g + j; after 16 mmas per slab the
-//     lane holds output columns 32q .. 32q+31 of rows g and g+8;
-//   * epilogue: with one K split the warp finishes the n-block itself; with
-//     several, it stores an fp32 partial, and the last warp to arrive on the
-//     n-block's counter sums the partials in split order (deterministic),
-//     applies had_r_128 over the 128 columns and sv, masks columns >= n_valid
-//     to -inf and writes y; it then resets the counter.
+// Up to three kernels per launch:
+//   1. rotate_frag_kernel: x' = RNE_fp16(had_r_128(x * su)) for the (<= 16)
+//      rows, written in mma fragment order (per 16-row k slab, lane (g, q)
+//      finds x'[g][4q..4q+3] and x'[g+8][4q..4q+3] as 8 or 16 contiguous
+//      bytes).
+//   2. decode_gemm_kernel: stream-K over all (n-block, k-slab) work. A slab
+//      is 16 k-rows x 128 output columns = 8 horizontally adjacent trellis
+//      tiles, 256*BITS contiguous bytes. The P = SMs x warps-per-CTA warps
+//      each own a contiguous range of slabs in n-block-major order, so every
+//      warp on every SM has the same amount of work. Each warp feeds itself:
+//      lane 0 streams its slabs (weights plus the slab's x' fragments) into a
+//      private ring in shared memory with cp.async.bulk, one mbarrier per
+//      stage.
+//      Lane (g, q) decodes tile g, rows 4q..4q+3 straight into m16n8k16 A
+//      fragments (A = W^T: mma row r <-> output column 16*(r%8) + j +
+//      8*(r/8) for mma j; mma k index 2q, 2q+1, 2q+8, 2q+9 <-> tile rows
+//      4q..4q+3, the same permutation x' was written in), B = x'^T (8 tokens
+//      per mma). After 8 mmas per slab and token group, lane (g, q) holds
+//      output columns 16g .. 16g+15 of tokens 2q, 2q+1 (+8).
+//      When a warp finishes its part of an n-block it either owns the whole
+//      n-block (then it applies had_r_128 over the 128 columns, sv and the
+//      -inf mask and writes y), or it stores an fp32 partial in its slot.
+//   3. decode_finalize_kernel (only when some n-block is shared): one warp
+//      per (n-block, row) sums the slots in slot order (deterministic),
+//      applies had_r_128, sv and the mask and writes y.
 //
-// Roofline: HBM-bound on the trellis bytes (K*N*BITS/8 per launch); the
-// per-weight integer decode is the competing ALU bound.
+// Roofline: HBM-bound on the trellis bytes (K*N*BITS/8 per launch) unless
+// the per-weight integer decode (a half-rate ALU pipe) binds first.
 #include <math.h>
 
 #include "exl3_common.cuh"
 #include "exl3_internal.h"
 
+// Tuning knobs (compile-time): warps per CTA for <= 8 rows, and which window
+// extractions use a high-half multiply (0: none, 1: word-aligned windows,
+// 2: word-aligned and nibble-offset-4 windows) instead of integer ALU ops.
+#ifndef EXL3_DECODE_WARPS_M8
+#define EXL3_DECODE_WARPS_M8 16
+#endif
+#ifndef EXL3_DECODE_MULHI_MODE
+#define EXL3_DECODE_MULHI_MODE 0
+#endif
+#ifndef EXL3_DECODE_STAGES_M8
+#define EXL3_DECODE_STAGES_M8 4
+#endif
+// Programmatic dependent launch between the rotation, decode and finalize
+// kernels (1: on).
+#ifndef EXL3_DECODE_PDL
+#define EXL3_DECODE_PDL 1
+#endif
+
 namespace exl3 {
 
 namespace {
 
-constexpr int NC = kDecodeConsumerWarps;
-
-template <int BITS>
+template <int BITS, int MT>
 struct DecodeCfg {
-  static constexpr int kSeg = 256 * BITS;                 // bytes of one 16x128 slab
-  static constexpr int kStages = BITS <= 4 ? 8 : 6;
-  static constexpr int kRingBytes = kStages * NC * kSeg;
+  static constexpr int kWarps = MT == 1 ? EXL3_DECODE_WARPS_M8 : 8;  // warps per CTA
+  static constexpr int kStages = MT == 1 ? EXL3_DECODE_STAGES_M8 : 6;  // ring stages per warp
+  static constexpr int kSeg = 256 * BITS;                    // trellis bytes per slab
+  static constexpr int kXB = 32 * 4 * MT * 2;                // x' fragment bytes per slab
+  static constexpr int kStage = kSeg;
+  static constexpr int kWarpRing = kStages * kStage;
+  static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8;
 };
 
 struct DecodeParams {
-  const __half *x;
   const uint8_t *trellis;
-  const __half *su;
+  const uint8_t *xf;  // rotated x in fragment order, K/16 slabs of 256*MT bytes
   const __half *sv;
   void *y;
   float *partials;
-  int *counters;
   int *status;
-  int64_t K, tiles_n, n_gemm, n_valid;
-  int rows, y_f32, NB, KB, S, Gs;
+  int64_t tiles_n, n_gemm, n_valid, TS, P;
+  int rows, y_f32, KT, smax;
+  uint32_t c65536;  // 65536, opaque to the compiler (keeps the shift on the FMA pipe)
 };
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Packed pair {w(state_a), w(state_b)}: both halves of each masked word are
+// summed with one fp16 add (operands selected by half), then the two sums are
+// packed. Same arithmetic as decode_pair, fewer integer-pipe instructions.
+__device__ __forceinline__ uint32_t decode_pair_sel(uint32_t state_a, uint32_t state_b) {
+  const uint32_t ua = lcg_word(state_a);
+  const uint32_t ub = lcg_word(state_b);
+  const __half2 ha = *reinterpret_cast<const __half2 *>(&ua);
+  const __half2 hb = *reinterpret_cast<const __half2 *>(&ub);
+  const __half2 r = __halves2half2(__hadd(__low2half(ha), __high2half(ha)), __hadd(__low2half(hb), __high2half(hb)));
+  return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// Output rotation + sv + mask + store of one 128-column block held as
-// v[rr][c] = row (g + 8 rr), column 32q + c, by lane (g, q).
-__device__ __forceinline__ void finish_block(float (&v)[2][32], const DecodeParams &p, int nb, int lane) {
-  const int g = lane >> 2, q = lane & 3;
+// Window states of a lane's four rows, for BITS = 4 with a nibble-shifted
+// copy of the words so that every state is one instruction.
+template <int BITS>
+struct Windows {
+  RowWindows<BITS> rw;
+  uint32_t X4[4 * BITS];
+  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
+    rw.build(own, prev);
+    if constexpr (BITS == 4) {
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (!(i & h)) {
-          float a = v[rr][i], b = v[rr][i + h];
-          v[rr][i] = a + b;
-          v[rr][i + h] = a - b;
-        }
-      }
-    }
-#pragma unroll
-    for (int s = 1; s < 4; s <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float o = __shfl_xor_sync(0xffffffffu, v[rr][i], s);
-        v[rr][i] = (q & s) ? (o - v[rr][i]) : (v[rr][i] + o);
-      }
+      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
+      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
     }
   }
-  const int64_t col0 = (int64_t)nb * 128 + 32 * q;
-  float scale[32];
+  // `k65536` holds 65536: a high-half product by it is the top 16 bits of a
+  // word, computed on the multiply pipe instead of the integer ALU.
+  template <int R, int C>
+  __device__ __forceinline__ uint32_t state(uint32_t k65536) const {
+    if constexpr (BITS == 4) {
+      constexpr int s = R * 64 + (C + 1) * 4;
+      constexpr int j = s >> 4;
+      constexpr int o = s & 15;
+      static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
+      static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
+      if constexpr (o == 0 && j < 4 * BITS && EXL3_DECODE_MULHI_MODE >= 1) {
+        return __umulhi(rw.X[j], k65536);  // seq[j], the top half of X[j]
+      } else if constexpr (o == 0) {
+        return rw.X[j - 1] & 0xFFFFu;      // seq[j], the low half of X[j-1]
+      } else if constexpr (o == 8) {
+        return __byte_perm(rw.X[j], 0u, 0x4421);
+      } else if constexpr (o == 4 && EXL3_DECODE_MULHI_MODE >= 2) {
+        return __umulhi(X4[j], k65536);
+      } else if constexpr (o == 4) {
+        return X4[j] >> 16;
+      } else {
+        return __byte_perm(X4[j], 0u, 0x4421);
+      }
+    } else {
+      return rw.template state<R, C>();
+    }
+  }
+};
+
+// Output rotation, sv, mask and store for the lane's values
+// v[mt][t][c] = token 8*mt + 2q + t, column nb*128 + 16g + c.
+template <int MT>
+__device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const DecodeParams &p, int64_t nb, int lane) {
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (!(i & h)) {
+            const float a = v[mt][t][i], b = v[mt][t][i + h];
+            v[mt][t][i] = a + b;
+            v[mt][t][i + h] = a - b;
+          }
+#pragma unroll
+      for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[mt][t][i], s * 4);
+          v[mt][t][i] = (g & s) ? (o - v[mt][t][i]) : (v[mt][t][i] + o);
+        }
+    }
+  const int64_t col0 = nb * 128 + 16 * g;
+  float scale[16];
   {
     const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      uint4 raw = __ldg(svp + a);
+    for (int a = 0; a < 2; ++a) {
+      const uint4 raw = __ldg(svp + a);
       const __half *h = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
       for (int e = 0; e < 8; ++e) scale[8 * a + e] = __half2float(h[e]) * kInvSqrt128;
     }
   }
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int m = g + 8 * rr;
-    float o[32];
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      o[c] = (col0 + c < p.n_valid) ? v[rr][c] * scale[c] : -INFINITY;
-    }
-    if (m < p.rows) {
-      if (p.y_f32) {
-        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + (int64_t)m * p.n_gemm + col0);
+    for (int t = 0; t < 2; ++t) {
+      const int m = 8 * mt + 2 * q + t;
+      float o[16];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) dst[a] = make_float4(o[4 * a], o[4 * a + 1], o[4 * a + 2], o[4 * a + 3]);
-      } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.y) + (int64_t)m * p.n_gemm + col0);
+      for (int c = 0; c < 16; ++c) o[c] = (col0 + c < p.n_valid) ? v[mt][t][c] * scale[c] : -INFINITY;
+      if (m < p.rows) {
+        if (p.y_f32) {
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + (int64_t)m * p.n_gemm + col0);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          uint32_t w[4];
+          for (int a = 0; a < 4; ++a) dst[a] = make_float4(o[4 * a], o[4 * a + 1], o[4 * a + 2], o[4 * a + 3]);
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.y) + (int64_t)m * p.n_gemm + col0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __half2 h2 = __floats2half2_rn(o[8 * a + 2 * e], o[8 * a + 2 * e + 1]);
-            w[e] = *reinterpret_cast<uint32_t *>(&h2);
+          for (int a = 0; a < 2; ++a) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __half2 h2 = __floats2half2_rn(o[8 * a + 2 * e], o[8 * a + 2 * e + 1]);
+              w[e] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            dst[a] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          dst[a] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
-  }
 }
 
-template <int BITS, int MROWS>
-__global__ void __launch_bounds__(32 * (1 + NC), 1) decode_gemm_kernel(const DecodeParams p) {
-  using Cfg = DecodeCfg<BITS>;
-  constexpr int kSeg = Cfg::kSeg;
-  constexpr int kStages = Cfg::kStages;
-  constexpr int CH = MROWS == 16 ? 8 : 4;  // fp16 A-fragment values per lane per k16 step
+__device__ __forceinline__ int64_t slab_owner(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
+
+// Waits until the preceding kernel in the stream has completed and its
+// memory is visible (no-op when launched without programmatic dependency).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream (if launched with programmatic
+// dependency) start its prologue now.
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <int BITS, int MT>
+__global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_gemm_kernel(const DecodeParams p) {
+  using Cfg = DecodeCfg<BITS, MT>;
+  constexpr int R = Cfg::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = blockIdx.x % p.S, gs = blockIdx.x / p.S;
-  const int kb0 = (int)((int64_t)ks * p.KB / p.S), kb1 = (int)((int64_t)(ks + 1) * p.KB / p.S);
-  const int nkb = kb1 - kb0;
-  const int T = nkb * 8;  // 16-row slabs in this K split
-  const int count = (p.NB - gs + p.Gs - 1) / p.Gs;
-  const int rounds = (count + NC - 1) / NC;
-  const int tmax = ((p.KB + p.S - 1) / p.S) * 8;
+  const int g = lane >> 2, q = lane & 3;
+  const int64_t pw = (int64_t)blockIdx.x * Cfg::kWarps + warp;
+  if (pw >= p.P) return;
+  const int64_t z0 = pw * p.TS / p.P, z1 = (pw + 1) * p.TS / p.P;
+  const int64_t nslab = z1 - z0;
 
-  __half *xs = reinterpret_cast<__half *>(smem);
-  uint8_t *ring = smem + align1024(tmax * 32 * CH * 2);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + Cfg::kRingBytes);
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), NC);
-    }
+  uint8_t *ring = smem + warp * Cfg::kWarpRing;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kWarps * Cfg::kWarpRing) + warp * R;
+  const uint32_t ring_s = smem_u32(ring);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < R; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_barrier_init();
   }
-  __syncthreads();
+  __syncwarp();
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      const uint32_t ring_s = smem_u32(ring);
-      for (int r = 0; r < rounds && ok; ++r) {
-        const int nvalid = min(NC, count - r * NC);
-        for (int t = 0; t < T; ++t) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(nvalid * kSeg));
-          const int64_t tk = (int64_t)kb0 * 8 + t;
-          for (int w = 0; w < nvalid; ++w) {
-            const int64_t nb = gs + (int64_t)(r * NC + w) * p.Gs;
-            const uint8_t *src = p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS);
-            bulk_g2s(ring_s + (uint32_t)((stage * NC + w) * kSeg), src, kSeg, full_bar(stage));
-          }
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // Every issued copy must land before the CTA may retire.
-      for (int s = 0; s < kStages; ++s) {
-        const int64_t uses = issued / kStages + (s < issued % kStages ? 1 : 0);
-        if (uses > 0) mbar_wait_short(full_bar(s), (uint32_t)((uses - 1) & 1));
-      }
+  // Issue cursor (used by lane 0 only): next slab to stream in, as (n-block,
+  // k slab, ring stage).
+  const int KT = p.KT;
+  int i_nb = (int)(z0 / KT), i_tk = (int)(z0 % KT), i_st = 0;
+  int64_t issued = 0;
+  const int64_t slab_stride = p.tiles_n * (32 * BITS);
+  auto issue_next = [&]() {
+    const uint32_t bar = smem_u32(&bars[i_st]);
+    mbar_arrive_expect_tx(bar, Cfg::kStage);
+    bulk_g2s(ring_s + i_st * Cfg::kStage, p.trellis + i_tk * slab_stride + (int64_t)i_nb * (8 * 32 * BITS),
+             Cfg::kSeg, bar);
+    if (++i_st == R) i_st = 0;
+    if (++i_tk == KT) {
+      i_tk = 0;
+      ++i_nb;
     }
-    return;
+    ++issued;
+  };
+  if (lane == 0) {
+    for (int64_t t = 0; t < R - 1 && t < nslab; ++t) issue_next();
   }
+  allow_next_grid();
+  wait_prior_grid();  // x' comes from the rotation kernel
 
-  // ---------------- consumers ----------------
-  const int cw = warp - 1;
-  const int g = lane >> 2, q = lane & 3;
+  float acc[MT][8][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
 
-  // Prologue: x' = RNE_fp16(had_r_128(x * su)) for this K split, stored so
-  // that lane (g, q) of k16 step t finds {x'[g][4q..4q+3], x'[g+8][4q..4q+3]}
-  // at xs[(t*32 + lane)*CH].
-  {
-    const int l16 = lane & 15;
-    const int jobs = MROWS * nkb;
-    for (int jp = cw; jp * 2 < jobs; jp += NC) {
-      const int job = jp * 2 + (lane >> 4);
-      const bool valid = job < jobs;
-      const int m = valid ? job / nkb : 0;
-      const int kbl = valid ? job % nkb : 0;
-      float v[8];
-      if (valid && m < p.rows) {
-        const int64_t kofs = (int64_t)(kb0 + kbl) * 128 + 8 * l16;
-        uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.x + (int64_t)m * p.K + kofs));
-        uint4 sraw = __ldg(reinterpret_cast<const uint4 *>(p.su + kofs));
-        const __half *h = reinterpret_cast<const __half *>(&raw);
-        const __half *sh = reinterpret_cast<const __half *>(&sraw);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __half2float(h[i]) * __half2float(sh[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
-      }
-#pragma unroll
-      for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (!(i & h)) {
-            float a = v[i], b = v[i + h];
-            v[i] = a + b;
-            v[i + h] = a - b;
-          }
-        }
-      }
-#pragma unroll
-      for (int s = 1; s < 16; s <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float o = __shfl_xor_sync(0xffffffffu, v[i], s);
-          v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
-        }
-      }
-      if (valid) {
-        __half2 hv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(v[2 * e] * kInvSqrt128, v[2 * e + 1] * kInvSqrt128);
-        const int t = kbl * 8 + (l16 >> 1);
-        const int qq = 2 * (l16 & 1);
-        const int gg = m & 7;
-        const int off = (m >= 8) ? 4 : 0;
-        __half *d0 = xs + (size_t)(t * 32 + gg * 4 + qq) * CH + off;
-        __half *d1 = xs + (size_t)(t * 32 + gg * 4 + qq + 1) * CH + off;
-        *reinterpret_cast<uint2 *>(d0) = make_uint2(*reinterpret_cast<uint32_t *>(&hv[0]),
-                                                    *reinterpret_cast<uint32_t *>(&hv[1]));
-        *reinterpret_cast<uint2 *>(d1) = make_uint2(*reinterpret_cast<uint32_t *>(&hv[2]),
-                                                    *reinterpret_cast<uint32_t *>(&hv[3]));
-      }
-    }
-  }
-  named_bar_sync(1, NC * 32);
-
-  int stage = 0;
+  // Consumer cursor.
+  int nb = (int)(z0 / KT), tk = (int)(z0 % KT), s = 0;
   uint32_t phase = 0;
-  for (int r = 0; r < rounds; ++r) {
-    const int i = r * NC + cw;
-    const bool valid = i < count;
-    const int nb = gs + i * p.Gs;
-    float acc[16][4];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
-
-    for (int t = 0; t < T; ++t) {
-      if (!mbar_wait(full_bar(stage), phase, p.status)) return;
-      if (valid) {
-        uint32_t own[2 * BITS];
-        load_own_words<BITS, true>(ring + (stage * NC + cw) * kSeg + lane * 8 * BITS, own);
-        const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-        RowWindows<BITS> rw;
-        rw.build(own, prev);
-        uint32_t a0, a1, a2, a3;
-        if constexpr (MROWS == 16) {
-          uint4 av = *reinterpret_cast<const uint4 *>(xs + (size_t)(t * 32 + lane) * CH);
-          a0 = av.x; a2 = av.y; a1 = av.z; a3 = av.w;
-        } else {
-          uint2 av = *reinterpret_cast<const uint2 *>(xs + (size_t)(t * 32 + lane) * CH);
-          a0 = av.x; a2 = av.y; a1 = 0u; a3 = 0u;
-        }
-        static_for<16>([&](auto C) {
-          const uint32_t b0 = decode_pair(rw.template state<0, C.value>(), rw.template state<1, C.value>());
-          const uint32_t b1 = decode_pair(rw.template state<2, C.value>(), rw.template state<3, C.value>());
-          mma16816(acc[C.value], a0, a1, a2, a3, b0, b1);
-        });
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(stage));
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+  // x' fragments of the current slab, loaded one slab ahead.
+  uint32_t bx[2 * MT], bx_next[2 * MT];
+  auto load_x = [&](int k_slab, uint32_t (&dst)[2 * MT]) {
+    if constexpr (MT == 1) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p.xf + (int64_t)k_slab * Cfg::kXB) + lane);
+      dst[0] = v.x;
+      dst[1] = v.y;
+    } else {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xf + (int64_t)k_slab * Cfg::kXB) + lane);
+      dst[0] = v.x;
+      dst[1] = v.y;
+      dst[2] = v.z;
+      dst[3] = v.w;
     }
-    if (!valid) continue;
-
-    float v[2][32];
-    if (p.S == 1) {
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          v[rr][c] = acc[c][2 * rr];
-          v[rr][c + 16] = acc[c][2 * rr + 1];
-        }
-      finish_block(v, p, nb, lane);
-      continue;
-    }
-    // Split K: publish this split's partial, then let the last arrival finish.
-    {
-      float *part = p.partials + (int64_t)ks * 16 * p.n_gemm + (int64_t)nb * 128 + 32 * q;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int m = g + 8 * rr;
-        if (m < p.rows) {
-          float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)m * p.n_gemm);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            dst[a] = make_float4(acc[4 * a][2 * rr], acc[4 * a + 1][2 * rr], acc[4 * a + 2][2 * rr],
-                                 acc[4 * a + 3][2 * rr]);
-            dst[a + 4] = make_float4(acc[4 * a][2 * rr + 1], acc[4 * a + 1][2 * rr + 1],
-                                     acc[4 * a + 2][2 * rr + 1], acc[4 * a + 3][2 * rr + 1]);
+  };
+  load_x(tk, bx_next);
+  for (int64_t t = 0; t < nslab; ++t) {
+    if (lane == 0 && issued < nslab) issue_next();
+    if (!mbar_wait(smem_u32(&bars[s]), phase, p.status)) {
+      if (lane == 0) {  // let this warp's copies in flight land before it retires
+        int ws = s;
+        uint32_t wp = phase;
+        for (int64_t u = t; u < issued; ++u) {
+          mbar_wait_short(smem_u32(&bars[ws]), wp);
+          if (++ws == R) {
+            ws = 0;
+            wp ^= 1u;
           }
         }
       }
+      return;
     }
-    __threadfence();
+    const uint8_t *stage = ring + s * Cfg::kStage;
+    uint32_t own[2 * BITS];
+    load_own_words<BITS, true>(stage + lane * 8 * BITS, own);
+#pragma unroll
+    for (int i = 0; i < 2 * MT; ++i) bx[i] = bx_next[i];
+    if (t + 1 < nslab) load_x(tk + 1 == KT ? 0 : tk + 1, bx_next);
+    const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
+    Windows<BITS> win;
+    win.build(own, prev);
+    static_for<8>([&](auto J) {
+      constexpr int j = J.value;
+      const uint32_t k = p.c65536;
+      const uint32_t a0 = decode_pair_sel(win.template state<0, j>(k), win.template state<1, j>(k));
+      const uint32_t a1 = decode_pair_sel(win.template state<0, j + 8>(k), win.template state<1, j + 8>(k));
+      const uint32_t a2 = decode_pair_sel(win.template state<2, j>(k), win.template state<3, j>(k));
+      const uint32_t a3 = decode_pair_sel(win.template state<2, j + 8>(k), win.template state<3, j + 8>(k));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
+    });
     __syncwarp();
-    int old = 0;
-    if (lane == 0) old = atomicAdd(&p.counters[nb], 1);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != p.S - 1) continue;
-    __threadfence();
+    fence_proxy_async_shared();  // our reads of this stage precede its next async refill
+    if (++s == R) {
+      s = 0;
+      phase ^= 1u;
+    }
+    const bool block_done = (tk == KT - 1) || (t == nslab - 1);
+    const int cur_nb = nb;
+    if (++tk == KT) {
+      tk = 0;
+      ++nb;
+    }
+    if (!block_done) continue;
+
+    // ---- this warp's part of n-block cnb is complete ----
+    const int64_t cnb = cur_nb;
+    float v[MT][2][16];
+    const bool whole = (z0 <= cnb * p.KT) && (z1 >= (cnb + 1) * p.KT);
+    if (whole) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) v[rr][c] = 0.f;
-    for (int s = 0; s < p.S; ++s) {
-      const float *part = p.partials + (int64_t)s * 16 * p.n_gemm + (int64_t)nb * 128 + 32 * q;
+        for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int m = g + 8 * rr;
-        if (m < p.rows) {
-          const float4 *src = reinterpret_cast<const float4 *>(part + (int64_t)m * p.n_gemm);
+          for (int c = 0; c < 8; ++c) {
+            v[mt][tt][c] = acc[mt][c][tt];
+            v[mt][tt][c + 8] = acc[mt][c][2 + tt];
+          }
+      finish_block<MT>(v, p, cnb, lane);
+    } else {
+      // Store this warp's contribution in its slot; decode_finalize_kernel
+      // sums the n-block's slots in slot order.
+      const int64_t pf = slab_owner(cnb * p.KT, p.P, p.TS);
+      const int64_t slot_elems = (int64_t)8 * MT * 128;
+      float *part = p.partials + (cnb * p.smax + (pw - pf)) * slot_elems;
 #pragma unroll
-          for (int a = 0; a < 8; ++a) {
-            float4 f = __ldcg(src + a);
-            v[rr][4 * a] += f.x;
-            v[rr][4 * a + 1] += f.y;
-            v[rr][4 * a + 2] += f.z;
-            v[rr][4 * a + 3] += f.w;
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          const int m = 8 * mt + 2 * q + tt;
+          if (m < p.rows) {
+            float4 *dst = reinterpret_cast<float4 *>(part + m * 128 + 16 * g);
+            dst[0] = make_float4(acc[mt][0][tt], acc[mt][1][tt], acc[mt][2][tt], acc[mt][3][tt]);
+            dst[1] = make_float4(acc[mt][4][tt], acc[mt][5][tt], acc[mt][6][tt], acc[mt][7][tt]);
+            dst[2] = make_float4(acc[mt][0][2 + tt], acc[mt][1][2 + tt], acc[mt][2][2 + tt], acc[mt][3][2 + tt]);
+            dst[3] = make_float4(acc[mt][4][2 + tt], acc[mt][5][2 + tt], acc[mt][6][2 + tt], acc[mt][7][2 + tt]);
           }
         }
-      }
     }
-    finish_block(v, p, nb, lane);
-    if (lane == 0) atomicExch(&p.counters[nb], 0);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
   }
 }
 
-template <int BITS, int MROWS>
-size_t smem_bytes_for(int tmax) {
-  constexpr int CH = MROWS == 16 ? 8 : 4;
-  return (size_t)align1024(tmax * 32 * CH * 2) + DecodeCfg<BITS>::kRingBytes +
-         2 * DecodeCfg<BITS>::kStages * sizeof(uint64_t);
+// Sums the partial slots of every n-block shared by several warps, in slot
+// order, then applies had_r_128 over the block's 128 columns, sv and the
+// -inf mask, and writes y. One warp per (n-block, row); lane l owns columns
+// 4l .. 4l+3. N-blocks owned by a single warp were finished by that warp.
+__global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__restrict__ partials, int64_t smax,
+                                                              int64_t slot_elems, const __half *__restrict__ sv,
+                                                              void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
+                                                              int rows, int64_t P, int64_t TS, int KT) {
+  wait_prior_grid();  // partial slots come from the decode kernel
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nb = w / rows;
+  const int m = (int)(w % rows);
+  if (nb >= n_gemm / 128) return;
+  const int64_t pf = slab_owner(nb * KT, P, TS);
+  const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
+  if (cnt == 1) return;
+  const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int sl = 0; sl < cnt; ++sl) {
+    const float4 f = __ldcg(reinterpret_cast<const float4 *>(base + sl * slot_elems));
+    v[0] += f.x;
+    v[1] += f.y;
+    v[2] += f.z;
+    v[3] += f.w;
+  }
+  {
+    float a = v[0], b = v[1];
+    v[0] = a + b;
+    v[1] = a - b;
+    a = v[2];
+    b = v[3];
+    v[2] = a + b;
+    v[3] = a - b;
+    a = v[0];
+    b = v[2];
+    v[0] = a + b;
+    v[2] = a - b;
+    a = v[1];
+    b = v[3];
+    v[1] = a + b;
+    v[3] = a - b;
+  }
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
+      v[i] = (lane & s) ? (o - v[i]) : (v[i] + o);
+    }
+  const int64_t col = nb * 128 + 4 * lane;
+  const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(sv + col));
+  const __half *sh = reinterpret_cast<const __half *>(&sraw);
+  float o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = (col + i < n_valid) ? v[i] * (__half2float(sh[i]) * kInvSqrt128) : -INFINITY;
+  if (y_f32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(y) + (int64_t)m * n_gemm + col) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+    __half2 h0 = __floats2half2_rn(o[0], o[1]), h1 = __floats2half2_rn(o[2], o[3]);
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + (int64_t)m * n_gemm + col) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+  }
 }
 
-template <int BITS, int MROWS>
+// x' = RNE_fp16(had_r_128(x * su)) for up to 8*MT rows, in fragment order:
+// for k slab tk, lane (g, q) owns 4*MT halves at xf[(tk*32 + 4g + q)*4*MT],
+// {x'[g][16tk+4q .. +3], x'[g+8][16tk+4q .. +3]}. Rows >= `rows` are zero.
+// One half-warp per (row, 128-block): lane l16 holds elements 8*l16 .. +7,
+// butterfly stages h = 1, 2, 4 in-lane and 8 .. 64 across lanes.
+template <int MT>
+__global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restrict__ x, const __half *__restrict__ su,
+                                                          int rows, int64_t K, __half *__restrict__ xf) {
+  constexpr int CH = 4 * MT;
+  allow_next_grid();
+  const int lane = threadIdx.x & 31, l16 = lane & 15;
+  const int64_t KB = K / 128;
+  const int64_t jobs = 8 * MT * KB;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t jp = warp; jp * 2 < jobs; jp += nwarps) {
+    const int64_t job = jp * 2 + (lane >> 4);
+    const bool valid = job < jobs;
+    const int m = valid ? (int)(job / KB) : 0;
+    const int64_t kb = valid ? job % KB : 0;
+    float v[8];
+    if (valid && m < rows) {
+      const int64_t k = kb * 128 + 8 * l16;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + k));
+      const uint4 sraw = __ldg(reinterpret_cast<const uint4 *>(su + k));
+      const __half *h = reinterpret_cast<const __half *>(&raw);
+      const __half *sh = reinterpret_cast<const __half *>(&sraw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __half2float(h[i]) * __half2float(sh[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!(i & h)) {
+          const float a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
+        v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
+      }
+    if (valid) {
+      __half2 hv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(v[2 * e] * kInvSqrt128, v[2 * e + 1] * kInvSqrt128);
+      const int64_t tk = kb * 8 + (l16 >> 1);
+      const int qq = 2 * (l16 & 1);
+      const int gg = m & 7;
+      const int off = (m >> 3) * 4;
+      __half *d0 = xf + (tk * 32 + gg * 4 + qq) * CH + off;
+      __half *d1 = xf + (tk * 32 + gg * 4 + qq + 1) * CH + off;
+      *reinterpret_cast<uint2 *>(d0) =
+          make_uint2(*reinterpret_cast<uint32_t *>(&hv[0]), *reinterpret_cast<uint32_t *>(&hv[1]));
+      *reinterpret_cast<uint2 *>(d1) =
+          make_uint2(*reinterpret_cast<uint32_t *>(&hv[2]), *reinterpret_cast<uint32_t *>(&hv[3]));
+    }
+  }
+}
+
+template <int BITS, int MT>
 cudaError_t init_one() {
-  const int tmax = (kDecodeMaxKSplit / 16);
-  return cudaFuncSetAttribute(decode_gemm_kernel<BITS, MROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes_for<BITS, MROWS>(tmax));
+  cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<BITS, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DecodeCfg<BITS, MT>::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes a;
+  e = cudaFuncGetAttributes(&a, decode_finalize_kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&a, rotate_frag_kernel<MT>);
 }
 
 template <int BITS>
 cudaError_t init_bits() {
-  cudaError_t e = init_one<BITS, 8>();
+  cudaError_t e = init_one<BITS, 1>();
   if (e != cudaSuccess) return e;
-  return init_one<BITS, 16>();
+  return init_one<BITS, 2>();
 }
 
-template <int BITS>
-cudaError_t launch_bits(const DecodeParams &dp, int tmax, cudaStream_t st) {
-  const unsigned grid = (unsigned)(dp.S * dp.Gs);
-  if (dp.rows <= 8) {
-    decode_gemm_kernel<BITS, 8><<<grid, 32 * (1 + NC), smem_bytes_for<BITS, 8>(tmax), st>>>(dp);
-  } else {
-    decode_gemm_kernel<BITS, 16><<<grid, 32 * (1 + NC), smem_bytes_for<BITS, 16>(tmax), st>>>(dp);
-  }
-  return cudaGetLastError();
+// Launches `kernel` after the previous work in `st`; with EXL3_DECODE_PDL its
+// prologue may overlap the tail of the previous kernel (programmatic
+// dependency), and the kernel itself waits before reading that kernel's
+// output.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = EXL3_DECODE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+template <int BITS, int MT>
+cudaError_t launch_bits(const DecodeParams &dp, int64_t grid, cudaStream_t st) {
+  return launch_dependent(decode_gemm_kernel<BITS, MT>, (unsigned)grid, DecodeCfg<BITS, MT>::kWarps * 32,
+                          DecodeCfg<BITS, MT>::kSmem, st, dp);
+}
+
+template <int MT>
+cudaError_t launch_mt(int bits, const DecodeParams &dp, int64_t grid, cudaStream_t st) {
+  switch (bits) {
+    case 2: return launch_bits<2, MT>(dp, grid, st);
+    case 3: return launch_bits<3, MT>(dp, grid, st);
+    case 4: return launch_bits<4, MT>(dp, grid, st);
+    case 5: return launch_bits<5, MT>(dp, grid, st);
+    case 6: return launch_bits<6, MT>(dp, grid, st);
+    case 8: return launch_bits<8, MT>(dp, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int64_t owner_host(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
 
 }  // namespace
 
 DecodePlan decode_plan(int64_t n_blocks, int64_t k_blocks, int num_sms) {
-  DecodePlan best;
-  int64_t best_cost = -1, best_grid = 0;
-  const int64_t s_min = ceil_div(k_blocks, kDecodeMaxKSplit / 128);
-  const int64_t s_max = k_blocks < 64 ? k_blocks : 64;
-  for (int64_t S = s_min; S <= s_max; ++S) {
-    if (S > num_sms) break;
-    const int64_t gs_max = n_blocks < num_sms / S ? n_blocks : num_sms / S;
-    for (int64_t Gs = 1; Gs <= gs_max; ++Gs) {
-      const int64_t rounds = ceil_div(ceil_div(n_blocks, Gs), NC);
-      const int64_t cost = rounds * ceil_div(k_blocks, S);
-      const int64_t grid = S * Gs;
-      if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > best_grid && S == best.S)) {
-        best_cost = cost;
-        best_grid = grid;
-        best.S = (int)S;
-        best.Gs = (int)Gs;
-      }
+  DecodePlan plan;
+  const int64_t KT = k_blocks * 8;
+  const int64_t TS = n_blocks * KT;
+  for (int mt = 1; mt <= 2; ++mt) {
+    const int warps = mt == 1 ? DecodeCfg<4, 1>::kWarps : DecodeCfg<4, 2>::kWarps;
+    int64_t P = (int64_t)num_sms * warps;
+    if (P > TS) P = TS;
+    int64_t smax = 1;
+    for (int64_t nb = 0; nb < n_blocks; ++nb) {
+      const int64_t c = owner_host((nb + 1) * KT - 1, P, TS) - owner_host(nb * KT, P, TS) + 1;
+      if (c > smax) smax = c;
     }
+    plan.P[mt - 1] = P;
+    plan.grid[mt - 1] = ceil_div(P, warps);
+    plan.smax[mt - 1] = smax;
   }
-  return best;
+  return plan;
+}
+
+size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks) {
+  const size_t a = (size_t)n_blocks * plan.smax[0] * 8 * 128 * 4;
+  const size_t b = (size_t)n_blocks * plan.smax[1] * 16 * 128 * 4;
+  return a > b ? a : b;
 }
 
 cudaError_t init_decode_kernels() {
@@ -448,35 +617,49 @@ cudaError_t init_decode_kernels() {
 }
 
 cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
+  const int MT = L.rows <= 8 ? 1 : 2;
+  const int64_t K = L.K;
+  // 1. rotated activations in fragment order
+  {
+    const int64_t jobs = 8 * MT * (K / 128);
+    int64_t grid = ceil_div(ceil_div(jobs, 2), 8);
+    if (MT == 1)
+      rotate_frag_kernel<1><<<(unsigned)grid, 256, 0, st>>>(static_cast<const __half *>(L.x),
+                                                            static_cast<const __half *>(L.su), L.rows, K,
+                                                            static_cast<__half *>(L.xf));
+    else
+      rotate_frag_kernel<2><<<(unsigned)grid, 256, 0, st>>>(static_cast<const __half *>(L.x),
+                                                            static_cast<const __half *>(L.su), L.rows, K,
+                                                            static_cast<__half *>(L.xf));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2. stream-K decode GEMM
   DecodeParams dp;
-  dp.x = static_cast<const __half *>(L.x);
   dp.trellis = reinterpret_cast<const uint8_t *>(L.trellis);
-  dp.su = static_cast<const __half *>(L.su);
+  dp.xf = static_cast<const uint8_t *>(L.xf);
   dp.sv = static_cast<const __half *>(L.sv);
   dp.y = L.y;
   dp.partials = L.partials;
-  dp.counters = L.counters;
   dp.status = L.status;
-  dp.K = L.K;
   dp.tiles_n = L.n_stored / 16;
   dp.n_gemm = L.n_gemm;
   dp.n_valid = L.n_valid;
+  dp.KT = (int)(K / 16);
+  dp.TS = (L.n_gemm / 128) * dp.KT;
+  dp.P = L.plan.P[MT - 1];
+  dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
   dp.y_f32 = L.y_f32;
-  dp.NB = (int)(L.n_gemm / 128);
-  dp.KB = (int)(L.K / 128);
-  dp.S = L.plan.S;
-  dp.Gs = L.plan.Gs;
-  const int tmax = (int)ceil_div(dp.KB, dp.S) * 8;
-  switch (L.bits) {
-    case 2: return launch_bits<2>(dp, tmax, st);
-    case 3: return launch_bits<3>(dp, tmax, st);
-    case 4: return launch_bits<4>(dp, tmax, st);
-    case 5: return launch_bits<5>(dp, tmax, st);
-    case 6: return launch_bits<6>(dp, tmax, st);
-    case 8: return launch_bits<8>(dp, tmax, st);
-    default: return cudaErrorInvalidValue;
-  }
+  dp.c65536 = 65536u;
+  const int64_t grid = L.plan.grid[MT - 1];
+  cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, grid, st) : launch_mt<2>(L.bits, dp, grid, st);
+  if (e != cudaSuccess || dp.smax == 1) return e;
+  // 3. reduce the slots of n-blocks shared by several warps
+  const int64_t warps = (L.n_gemm / 128) * L.rows;
+  return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st,
+                          (const float *)L.partials, (int64_t)dp.smax, (int64_t)8 * MT * 128, dp.sv, L.y, L.y_f32,
+                          L.n_gemm, L.n_valid, L.rows, dp.P, dp.TS, dp.KT);
 }
 
 }  // namespace exl3

@@ -14,18 +14,21 @@ constexpr int kDecodeRows = 16;           // activation rows per decode-GEMM lau
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Split-K / n-block assignment of the decode-shaped GEMM.
+// Stream-K assignment of the decode-shaped GEMM, per token-group variant
+// (index 0: <= 8 rows, index 1: <= 16 rows): P warps in total over `grid`
+// CTAs, at most smax partial slots per 128-column n-block.
 struct DecodePlan {
-  int S = 1;   // K splits (each a whole number of 128-row blocks)
-  int Gs = 1;  // CTAs per split; CTA (ks, gs) owns n-blocks gs, gs+Gs, ...
-  int grid() const { return S * Gs; }
+  int64_t P[2] = {1, 1};
+  int64_t grid[2] = {1, 1};
+  int64_t smax[2] = {1, 1};
 };
 DecodePlan decode_plan(int64_t n_blocks, int64_t k_blocks, int num_sms);
+size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks);
 
 // Workspace layout shared by the size query and the calls.
 struct WorkspaceLayout {
   DecodePlan plan;
-  size_t counters_off = 0, partials_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
+  size_t partials_off = 0, xf_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
   int64_t xr_rows = 0;      // rows of the rotated-activation buffer (multiple of 128)
   int64_t chunk_rows = 0;   // rows of the reconstruct chunk (multiple of 256)
   bool prefill = false;
@@ -43,8 +46,8 @@ struct DecodeLaunch {
   const void *su, *sv;
   void *y;                // rows m0.. of y, ld = n_gemm
   int y_f32;
-  float *partials;        // S x 16 x n_gemm fp32 (unused when S == 1)
-  int *counters;          // n_gemm/128 int32, zero between calls
+  void *xf;               // rotated rows in mma fragment order, K * 32 bytes
+  float *partials;        // n-blocks x smax slots x (8 or 16) x 128 fp32
   int *status;
   DecodePlan plan;
 };

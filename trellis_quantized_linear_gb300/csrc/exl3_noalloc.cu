@@ -1,6 +1,6 @@
 // Decode-shaped linear layer for callers that cannot allocate device memory.
 //
-// The split-K partial sums and the completion counters that exl3_linear
+// The rotated activations and the split-K partial sums that exl3_linear
 // keeps in the caller's workspace live here in one fixed, file-scope device
 // array instead. In host code the array's name is only a host-side stand-in,
 // so its device address is looked up once per device (with that device
@@ -60,9 +60,6 @@ extern "C" exl3_status exl3_linear_decode_noalloc(const void *x, int64_t M, int6
   uint8_t *ws = scratch_on_current_device();
   if (!ws) return EXL3_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The counters must start at zero; an earlier call may have been cut short.
-  if (cudaMemsetAsync(ws + L.counters_off, 0, (size_t)(n_gemm / 128) * sizeof(int), st) != cudaSuccess)
-    return EXL3_ERR_CUDA;
   const size_t ysz = y_dtype == EXL3_F32 ? 4 : 2;
   for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
     DecodeLaunch d;
@@ -78,8 +75,8 @@ extern "C" exl3_status exl3_linear_decode_noalloc(const void *x, int64_t M, int6
     d.sv = sv;
     d.y = static_cast<uint8_t *>(y) + (size_t)(m0 * n_gemm) * ysz;
     d.y_f32 = y_dtype == EXL3_F32;
+    d.xf = ws + L.xf_off;
     d.partials = reinterpret_cast<float *>(ws + L.partials_off);
-    d.counters = reinterpret_cast<int *>(ws + L.counters_off);
     d.status = dev->status;
     d.plan = L.plan;
     if (launch_decode_gemm(d, st) != cudaSuccess) return EXL3_ERR_CUDA;
