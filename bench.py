@@ -12,7 +12,9 @@ Also measured in the same run (reported as sub-objects of the JSON line):
               (TFLOP/s = 2*M*K*N / call time, reconstruct and Hadamards
               included), with the reconstruct / GEMM split;
   crossover - both paths timed at M in {64 .. 4096} on both MLP geometries;
-  logits    - the odd-vocab masked logits call at M in {1, 16, 2048}.
+  logits    - the odd-vocab masked logits call at M in {1, 16, 2048};
+  mlp_stack - 64 dense MLP layers (gate, up, SiLU*up, down) at M=2048,
+              bits 4 and 3: ms per pass and the reconstruct/GEMM split.
 
 --impl reference times the CPU oracle (test infrastructure) on the host's
 cores on a bounded sample of the same workload, as the reference arm.
@@ -67,6 +69,21 @@ def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def reduce_max(torch, value: float, device) -> float:
+    """Max of `value` over all ranks (identity when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput of N independent replicas: the units all ranks
+    processed divided by the slowest rank's time."""
+    return units_per_rank * world / seconds_max
 
 
 def load_peaks():
@@ -278,13 +295,9 @@ def bench_decode(args, torch, tql, peaks, dist):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(torch, start.elapsed_time(end), "cuda")
     ms_per_step = ms / args.steps
-    value = per_step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(per_step_bytes, world, ms_per_step * 1e-3) / 1e9
 
     # per-M kernel durations (graph of 12 back-to-back launches of one shape)
     per_m = {}
@@ -378,7 +391,7 @@ def bench_prefill(args, torch, tql, peaks):
 
 def bench_crossover(args, torch, tql):
     out = {}
-    Ms = (64, 128, 256, 1024) if args.quick else synthetic.PREFILL_MS
+    Ms = (16, 32, 64, 128) if args.quick else (16, 32, 48) + tuple(synthetic.PREFILL_MS)
     for gm in synthetic.PREFILL_GEOMS:
         K, N, bits = gm["K"], gm["N"], 4
         mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
@@ -421,6 +434,81 @@ def bench_logits(args, torch, tql, peaks):
             r["frac_hbm"] = round(r["weight_gbs"] / peaks["hbm_gbs"], 4)
         res[str(M)] = r
     return res
+
+
+def bench_mlp_stack(args, torch, tql):
+    """64 layers of gate/up (5120->17408), SiLU(gate)*up, down (17408->5120)
+    at M=2048 on the prefill path, for bits 4 and 3. Weights are drawn on the
+    device (timing only); the per-layer parity of this geometry is covered by
+    the test suite with the host generator."""
+    st = synthetic.MLP_STACK
+    L, d, f, M = st["layers"], st["d_model"], st["d_ff"], st["M"]
+    if args.quick:
+        L = 8
+    out = {}
+    thr = 128
+    for bits in st["bits"]:
+        layers = []
+        for l in range(L):
+            mats = []
+            for j, (K, N) in enumerate(((d, f), (d, f), (f, d))):
+                tr, su, sv = synthetic.make_matrix_device(K, N, bits, seed=st["seed_base"] + l, matrix_index=j)
+                mats.append(dict(K=K, N=N, tr=tr, su=su, sv=sv))
+            layers.append(mats)
+        ws = torch.empty(max(tql.exl3_linear_workspace_bytes(M, d, f, bits, thr),
+                             tql.exl3_linear_workspace_bytes(M, f, d, bits, thr)), dtype=torch.uint8, device="cuda")
+        tql.exl3_workspace_init(ws)
+        x0 = _dev(torch, synthetic.make_activations(M, d, seed=st["seed_base"]))
+        g = torch.empty((M, f), dtype=torch.float16, device="cuda")
+        u = torch.empty_like(g)
+        h = torch.empty_like(g)
+        xa = torch.empty((M, d), dtype=torch.float16, device="cuda")
+
+        def lin(xin, m, yout):
+            tql.exl3_linear(xin, M, m["K"], m["tr"], bits, m["N"], m["N"], m["su"], m["sv"], yout, tql.EXL3_F16,
+                            thr, ws)
+
+        def one_pass(check=False):
+            xin = x0
+            first_bad = None
+            for l, (mg, mu, md) in enumerate(layers):
+                lin(xin, mg, g)
+                lin(xin, mu, u)
+                tql.exl3_silu_mul(g, u, h)
+                lin(h, md, xa)
+                xin = xa
+                if check and first_bad is None and not bool(torch.isfinite(xa).all()):
+                    first_bad = l
+            return first_bad
+
+        first_bad = one_pass(check=True)
+        torch.cuda.synchronize()
+        ms = time_fn(torch, one_pass, 2, 1)
+        # split from component timings of each geometry
+        split = {"hadamard": 0.0, "reconstruct": 0.0, "gemm": 0.0}
+        for (K, N), times in (((d, f), 2), ((f, d), 1)):
+            m = layers[0][0 if K == d else 2]
+            xin = x0 if K == d else h
+            yv = g if K == d else xa
+            t_call = time_fn(torch, lambda: lin(xin, m, yv), 5, 2)
+            xr = torch.empty((M, K), dtype=torch.float16, device="cuda")
+            t_had = time_fn(torch, lambda: tql.exl3_hadamard128(xin, xr, m["su"]), 5, 2)
+            wt = torch.empty((N, K), dtype=torch.float16, device="cuda")
+            t_rec = time_fn(torch, lambda: tql.exl3_reconstruct(m["tr"], bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK),
+                            5, 2)
+            split["hadamard"] += L * times * t_had
+            split["reconstruct"] += L * times * t_rec
+            split["gemm"] += L * times * (t_call - t_had - t_rec)
+            del xr, wt
+        flops = 2.0 * M * (2 * d * f + f * d) * L
+        out[f"bits{bits}"] = {"layers": L, "ms_per_pass": round(ms, 3), "tok_per_s": round(M / (ms * 1e-3), 1),
+                              "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                              "split_ms": {k: round(v, 3) for k, v in split.items()},
+                              "first_nonfinite_layer": first_bad,
+                              "trellis_gb": round(sum(m["tr"].numel() * 2 for lay in layers for m in lay) / 1e9, 2)}
+        del layers, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -506,7 +594,8 @@ def main():
     if not args.no_extras and rank == 0:
         for name, fn in (("prefill", lambda: bench_prefill(args, torch, tql, peaks)),
                          ("crossover", lambda: bench_crossover(args, torch, tql)),
-                         ("logits", lambda: bench_logits(args, torch, tql, peaks))):
+                         ("logits", lambda: bench_logits(args, torch, tql, peaks)),
+                         ("mlp_stack", lambda: bench_mlp_stack(args, torch, tql))):
             try:
                 extras[name] = fn()
             except Exception as ex:  # report, never hide

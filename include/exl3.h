@@ -42,7 +42,7 @@
  *     current, before any other call that touches it and before any CUDA
  *     graph capture: it loads every kernel and sets their attributes, so
  *     no later call loads modules, allocates or queries the device.
- *   - Supported trellis widths: bits in {2, 3, 4, 5, 6, 8}.
+ *   - Supported trellis widths: bits in 1..8.
  *   - Shapes: K % 128 == 0, n_gemm % 128 == 0, n_gemm <= n_stored,
  *     n_stored % 128 == 0.
  */
@@ -206,6 +206,14 @@ exl3_status exl3_logits_masked(const void *x, int64_t M, int64_t K, const uint16
  * bounded waits since the last read, EXL3_OK otherwise.
  */
 exl3_status exl3_get_device_status(void *stream);
+
+/*
+ * exl3_silu_mul: out = RNE_fp16(silu(gate) * up) elementwise (fp32 math,
+ * silu(a) = a / (1 + exp(-a))), n % 8 == 0. The glue between the gate/up
+ * and down projections of a dense MLP ([P1] follow-up comment: gate + up +
+ * down per layer); not itself part of the trellis layer.
+ */
+exl3_status exl3_silu_mul(const void *gate, const void *up, void *out, int64_t n, void *stream);
 
 /*
  * Self-test of the failure-detection path: launches one kernel that waits

@@ -80,3 +80,20 @@ MLP_STACK = dict(layers=64, d_model=5120, d_ff=17408, M=2048, bits=(3, 4), seed_
 LOGITS = dict(name="odd-vocab logits K=5120 n_stored=248320 n_gemm=248192 n_decodable=248077 bits=6",
               K=5120, n_stored=248320, n_gemm=248192, n_decodable=248077, bits=6,
               Ms=(1, 16, 2048), seed=4, chunk=32768)
+
+
+def make_matrix_device(K: int, n_stored: int, bits: int, seed: int, matrix_index: int = 0, device="cuda"):
+    """Timing-only stand-in for make_matrix drawn on the device with torch's
+    seeded generator (same shapes and distributions, different stream): used
+    where host generation of many gigabytes would dominate a benchmark.
+    Returns (trellis int16, su fp16, sv fp16) device tensors."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + int(matrix_index))
+    n_words = trellis_num_words(K, n_stored, bits)
+    trellis = torch.randint(-32768, 32768, (n_words,), generator=g, device=device, dtype=torch.int32).to(torch.int16)
+    su = torch.where(torch.randint(0, 2, (K,), generator=g, device=device) == 1, 1.0, -1.0).to(torch.float16)
+    sign = torch.where(torch.randint(0, 2, (n_stored,), generator=g, device=device) == 1, 1.0, -1.0)
+    mag = torch.rand((n_stored,), generator=g, device=device, dtype=torch.float64) * 0.015 + 0.005
+    sv = (sign.double() * mag).to(torch.float16)
+    return trellis, su, sv

@@ -50,7 +50,7 @@ def test_status_strings(lib):
 
 
 def test_supported_bits(lib):
-    assert [b for b in range(0, 10) if tql.exl3_supported_bits(b)] == [2, 3, 4, 5, 6, 8]
+    assert [b for b in range(0, 10) if tql.exl3_supported_bits(b)] == [1, 2, 3, 4, 5, 6, 7, 8]
 
 
 def test_logits_width_matches_page_example(lib):
@@ -128,7 +128,8 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert L.exl3_linear(good, 4, 128, good, 4, 256, 256, good, good, good, 1, -1, good, 1 << 30, None) == 1
     assert L.exl3_linear(good, -1, 128, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 1
     # unsupported bits
-    assert L.exl3_linear(good, 4, 128, good, 7, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 3
+    assert L.exl3_linear(good, 4, 128, good, 9, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 3
+    assert L.exl3_linear(good, 4, 128, good, 0, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 3
     # misaligned / null pointers
     assert L.exl3_linear(good + 2, 4, 128, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 2
     assert L.exl3_linear(good, 4, 128, None, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 2

@@ -59,7 +59,7 @@ def test_hadamard128_in_place(oracle):
 # reconstruct
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("layout", [tql.EXL3_LAYOUT_KN, tql.EXL3_LAYOUT_NK])
 @pytest.mark.parametrize("n0,n_cols", [(0, 640), (256, 256)])
 def test_reconstruct_bit_exact(oracle, bits, layout, n0, n_cols):
@@ -102,7 +102,7 @@ DECODE, PREFILL = 0, 1  # m_threshold values that force each path
 
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (128, 256, 3), (640, 384, 6), (256, 768, 2),
-                                      (384, 256, 5), (256, 256, 8)])
+                                      (384, 256, 5), (256, 256, 8), (256, 384, 1), (384, 384, 7)])
 @pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 37])
 def test_linear_decode_path(oracle, K, N, bits, M):
     m = synthetic.make_matrix(K, N, bits, seed=K + N + bits)
@@ -113,7 +113,7 @@ def test_linear_decode_path(oracle, K, N, bits, M):
     assert rel_err(y, ref) <= TOL
 
 
-@pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6)])
+@pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (256, 256, 1), (384, 256, 7)])
 @pytest.mark.parametrize("M", [1, 32, 130, 256])
 def test_linear_prefill_path(oracle, K, N, bits, M):
     m = synthetic.make_matrix(K, N, bits, seed=K * 3 + N + bits)
@@ -277,6 +277,38 @@ def test_logits_full_size_argmax_against_oracle(oracle):
     assert rel_err(lgn[fin], ref[fin]) <= TOL
     rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
     argmax_agrees(am.cpu().numpy(), ref, 2 * TOL * rms)
+
+
+def test_silu_mul_glue():
+    torch = torch_mod()
+    g = synthetic.make_activations(7, 384, seed=31)
+    u = synthetic.make_activations(7, 384, seed=32)
+    out = torch.empty((7, 384), dtype=torch.float16, device="cuda")
+    tql.exl3_silu_mul(to_dev(g), to_dev(u), out)
+    torch.cuda.synchronize()
+    a = g.astype(np.float64)
+    ref = (a / (1.0 + np.exp(-a)) * u.astype(np.float64)).astype(np.float16).astype(np.float64)
+    got = out.cpu().numpy().astype(np.float64)
+    ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= ulp)
+
+
+@pytest.mark.parametrize("layer", [0, 31, 63])
+@pytest.mark.parametrize("bits", [3, 4])
+def test_mlp_stack_layers_sampled(oracle, layer, bits):
+    """Dense MLP stack geometry: each layer's gate, up and down projections on
+    fresh N(0,1) input at M=2048 (prefill path), 128 sampled rows x 2 column
+    blocks checked against the oracle."""
+    st = synthetic.MLP_STACK
+    d, f, M = st["d_model"], st["d_ff"], st["M"]
+    rows = np.arange(0, M, M // 128)
+    for j, (K, N) in enumerate(((d, f), (d, f), (f, d))):
+        m = synthetic.make_matrix(K, N, bits, seed=st["seed_base"] + layer, matrix_index=j)
+        x = synthetic.make_activations(M, K, seed=st["seed_base"])
+        y = Layer(m).linear(to_dev(x), 128).cpu().numpy()
+        for b in (0, N // 128 - 1):
+            ref = oracle.linear(x[rows], m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
+            assert rel_err(y[rows, 128 * b:128 * b + 128], ref) <= TOL, (j, b)
 
 
 # ---------------------------------------------------------------------------

@@ -18,7 +18,7 @@ __all__ = [
     "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_linear_workspace_bytes_for",
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
-    "exl3_linear_decode_noalloc", "HEADER_SYMBOLS",
+    "exl3_linear_decode_noalloc", "exl3_silu_mul", "HEADER_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +42,7 @@ HEADER_SYMBOLS = (
     "exl3_decode_plan", "exl3_linear_workspace_bytes_for", "exl3_linear_workspace_bytes",
     "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct", "exl3_linear",
     "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
-    "exl3_linear_decode_noalloc",
+    "exl3_linear_decode_noalloc", "exl3_silu_mul",
 )
 
 
@@ -92,6 +92,7 @@ def load():
                                                   _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp]),
             "exl3_get_device_status": (ctypes.c_int, [_vp]),
             "exl3_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _vp]),
+            "exl3_silu_mul": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
             "exl3_linear_decode_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i64, _vp, _vp,
                                                           _vp, ctypes.c_int, _vp]),
         }
@@ -219,3 +220,9 @@ def exl3_linear_decode_noalloc(x, M: int, K: int, trellis, bits: int, n_stored: 
     _check(load().exl3_linear_decode_noalloc(_ptr(x), int(M), int(K), _ptr(trellis), int(bits), int(n_stored),
                                              int(n_gemm), _ptr(su), _ptr(sv), _ptr(y), int(y_dtype),
                                              _stream(stream)), "exl3_linear_decode_noalloc")
+
+
+def exl3_silu_mul(gate, up, out, n: int | None = None, stream=None) -> None:
+    """out = fp16(silu(gate) * up), the dense-MLP glue between projections."""
+    n = gate.numel() if n is None else n
+    _check(load().exl3_silu_mul(_ptr(gate), _ptr(up), _ptr(out), int(n), _stream(stream)), "exl3_silu_mul")

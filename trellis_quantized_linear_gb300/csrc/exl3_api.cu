@@ -121,9 +121,7 @@ exl3_status validate_linear(const void *x, int64_t M, int64_t K, const uint16_t 
 
 const DeviceInfo *initialized_device() { return current_device(); }
 
-bool bits_supported(int bits) {
-  return bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8;
-}
+bool bits_supported(int bits) { return bits >= 1 && bits <= 8; }
 
 bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold, int num_sms,
                       WorkspaceLayout *out) {
@@ -291,6 +289,14 @@ exl3_status exl3_logits_masked(const void *x, int64_t M, int64_t K, const uint16
                  m_threshold, static_cast<uint8_t *>(workspace), st);
   if (s != EXL3_OK) return s;
   return from_cuda(launch_argmax(logits, M, n_gemm, argmax, st));
+}
+
+exl3_status exl3_silu_mul(const void *gate, const void *up, void *out, int64_t n, void *stream) {
+  if (n < 0 || n % 8) return EXL3_ERR_INVALID_ARG;
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(out)) return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(launch_silu_mul(gate, up, out, n, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream) {

@@ -48,6 +48,14 @@
 #ifndef EXL3_DECODE_MULHI_MODE
 #define EXL3_DECODE_MULHI_MODE 0
 #endif
+// Packing of two decoded fp16 weights into one mma register, per variant
+// (0: byte permute on the integer pipe; 1: multiply-add on the fp16 pipe).
+#ifndef EXL3_DECODE_PACK_FMA_M8
+#define EXL3_DECODE_PACK_FMA_M8 0
+#endif
+#ifndef EXL3_DECODE_PACK_FMA_M16
+#define EXL3_DECODE_PACK_FMA_M16 1
+#endif
 #ifndef EXL3_DECODE_STAGES_M8
 #define EXL3_DECODE_STAGES_M8 4
 #endif
@@ -95,12 +103,23 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // Packed pair {w(state_a), w(state_b)}: both halves of each masked word are
 // summed with one fp16 add (operands selected by half), then the two sums are
 // packed. Same arithmetic as decode_pair, fewer integer-pipe instructions.
+template <bool kPackFma>
 __device__ __forceinline__ uint32_t decode_pair_sel(uint32_t state_a, uint32_t state_b) {
   const uint32_t ua = lcg_word(state_a);
   const uint32_t ub = lcg_word(state_b);
   const __half2 ha = *reinterpret_cast<const __half2 *>(&ua);
   const __half2 hb = *reinterpret_cast<const __half2 *>(&ub);
-  const __half2 r = __halves2half2(__hadd(__low2half(ha), __high2half(ha)), __hadd(__low2half(hb), __high2half(hb)));
+  __half2 r;
+  if constexpr (kPackFma) {
+  // (w_a, w_a) * (1, 0) + (w_b, w_b) * (0, 1): exact, no integer-pipe op.
+  const __half2 ra = __half2half2(__hadd(__low2half(ha), __high2half(ha)));
+  const __half2 rb = __half2half2(__hadd(__low2half(hb), __high2half(hb)));
+  const __half2 one_zero = __halves2half2(__float2half_rn(1.f), __float2half_rn(0.f));
+  const __half2 zero_one = __halves2half2(__float2half_rn(0.f), __float2half_rn(1.f));
+  r = __hfma2(ra, one_zero, __hmul2(rb, zero_one));
+  } else {
+  r = __halves2half2(__hadd(__low2half(ha), __high2half(ha)), __hadd(__low2half(hb), __high2half(hb)));
+  }
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
@@ -323,10 +342,11 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
     static_for<8>([&](auto J) {
       constexpr int j = J.value;
       const uint32_t k = p.c65536;
-      const uint32_t a0 = decode_pair_sel(win.template state<0, j>(k), win.template state<1, j>(k));
-      const uint32_t a1 = decode_pair_sel(win.template state<0, j + 8>(k), win.template state<1, j + 8>(k));
-      const uint32_t a2 = decode_pair_sel(win.template state<2, j>(k), win.template state<3, j>(k));
-      const uint32_t a3 = decode_pair_sel(win.template state<2, j + 8>(k), win.template state<3, j + 8>(k));
+      constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
+      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(k), win.template state<1, j>(k));
+      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(k), win.template state<1, j + 8>(k));
+      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(k), win.template state<3, j>(k));
+      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(k), win.template state<3, j + 8>(k));
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
     });
@@ -405,13 +425,19 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   if (cnt == 1) return;
   const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int sl = 0; sl < cnt; ++sl) {
-    const float4 f = __ldcg(reinterpret_cast<const float4 *>(base + sl * slot_elems));
-    v[0] += f.x;
-    v[1] += f.y;
-    v[2] += f.z;
-    v[3] += f.w;
+  for (int s0 = 0; s0 < cnt; s0 += 16) {
+    float4 f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)  // all loads of the chunk in flight at once
+      f[i] = (s0 + i < cnt) ? __ldcg(reinterpret_cast<const float4 *>(base + (s0 + i) * slot_elems))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // summed in slot order
+      v[0] += f[i].x;
+      v[1] += f[i].y;
+      v[2] += f[i].z;
+      v[3] += f[i].w;
+    }
   }
   {
     float a = v[0], b = v[1];
@@ -566,6 +592,8 @@ cudaError_t launch_bits(const DecodeParams &dp, int64_t grid, cudaStream_t st) {
 template <int MT>
 cudaError_t launch_mt(int bits, const DecodeParams &dp, int64_t grid, cudaStream_t st) {
   switch (bits) {
+    case 1: return launch_bits<1, MT>(dp, grid, st);
+    case 7: return launch_bits<7, MT>(dp, grid, st);
     case 2: return launch_bits<2, MT>(dp, grid, st);
     case 3: return launch_bits<3, MT>(dp, grid, st);
     case 4: return launch_bits<4, MT>(dp, grid, st);
@@ -608,6 +636,8 @@ size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks) {
 
 cudaError_t init_decode_kernels() {
   cudaError_t e;
+  if ((e = init_bits<1>()) != cudaSuccess) return e;
+  if ((e = init_bits<7>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
   if ((e = init_bits<4>()) != cudaSuccess) return e;

@@ -86,6 +86,7 @@ bool bits_supported(int bits);
 struct DeviceInfo;
 // The current device's cached set-up, or nullptr before exl3_init.
 const DeviceInfo *initialized_device();
+cudaError_t launch_silu_mul(const void *gate, const void *up, void *out, int64_t n, int num_sms, cudaStream_t st);
 cudaError_t launch_wait_timeout_selftest(int *status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace exl3

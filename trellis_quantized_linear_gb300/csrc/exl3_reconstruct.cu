@@ -75,6 +75,8 @@ static cudaError_t init_bits() {
 
 cudaError_t init_reconstruct_kernels() {
   cudaError_t e;
+  if ((e = init_bits<1>()) != cudaSuccess) return e;
+  if ((e = init_bits<7>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
   if ((e = init_bits<4>()) != cudaSuccess) return e;
@@ -106,6 +108,8 @@ cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int
   __half *wp = static_cast<__half *>(w);
   const int64_t tiles_n = n_stored / 16, nb0 = n0 / 128;
   switch (bits) {
+    case 1: launch_bits<1>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
+    case 7: launch_bits<7>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
     case 2: launch_bits<2>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
     case 3: launch_bits<3>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
     case 4: launch_bits<4>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;

@@ -142,11 +142,42 @@ cudaError_t launch_wait_timeout_selftest(int *status, unsigned long long limit_n
   return cudaGetLastError();
 }
 
+// out = RNE_fp16(silu(gate) * up), computed in fp32, 8 elements per thread.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const __half *__restrict__ gate, const __half *__restrict__ up,
+                                                       __half *__restrict__ out, int64_t n8) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 g = __ldg(reinterpret_cast<const uint4 *>(gate) + i);
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(up) + i);
+    const __half *gh = reinterpret_cast<const __half *>(&g);
+    const __half *uh = reinterpret_cast<const __half *>(&u);
+    uint4 r;
+    __half *rh = reinterpret_cast<__half *>(&r);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float a = __half2float(gh[e]);
+      rh[e] = __float2half_rn(a / (1.0f + __expf(-a)) * __half2float(uh[e]));
+    }
+    reinterpret_cast<uint4 *>(out)[i] = r;
+  }
+}
+
+cudaError_t launch_silu_mul(const void *gate, const void *up, void *out, int64_t n, int num_sms, cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  int64_t grid = ceil_div(n8, 256);
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  silu_mul_kernel<<<(unsigned)grid, 256, 0, st>>>(static_cast<const __half *>(gate), static_cast<const __half *>(up),
+                                                  static_cast<__half *>(out), n8);
+  return cudaGetLastError();
+}
+
 cudaError_t init_rotate_kernels() {
   cudaFuncAttributes a;
   cudaError_t e = cudaFuncGetAttributes(&a, hadamard128_kernel);
   if (e != cudaSuccess) return e;
   e = cudaFuncGetAttributes(&a, wait_timeout_selftest_kernel);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncGetAttributes(&a, silu_mul_kernel);
   if (e != cudaSuccess) return e;
   return cudaFuncGetAttributes(&a, argmax_rows_kernel);
 }
