@@ -34,6 +34,7 @@
 //
 // Roofline: HBM-bound on the trellis bytes (K*N*BITS/8 per launch) unless
 // the per-weight integer decode (a half-rate ALU pipe) binds first.
+#include <cuda.h>
 #include <math.h>
 
 #include "exl3_common.cuh"
@@ -57,7 +58,13 @@
 #define EXL3_DECODE_PACK_FMA_M16 1
 #endif
 #ifndef EXL3_DECODE_STAGES_M8
-#define EXL3_DECODE_STAGES_M8 4
+#define EXL3_DECODE_STAGES_M8 2
+#endif
+// Proxy fence after reading a ring stage (1) or none (0): the stage's words
+// are consumed by register-dependent decode work before the warp reaches the
+// reissue point, so the reuse is ordered without it.
+#ifndef EXL3_DECODE_PROXY_FENCE
+#define EXL3_DECODE_PROXY_FENCE 0
 #endif
 // Programmatic dependent launch between the rotation, decode and finalize
 // kernels (1: on).
@@ -69,13 +76,18 @@ namespace exl3 {
 
 namespace {
 
+#ifndef EXL3_DECODE_CHUNK
+#define EXL3_DECODE_CHUNK 4  // slabs per copy for BITS <= 4 (half that above)
+#endif
+
 template <int BITS, int MT>
 struct DecodeCfg {
   static constexpr int kWarps = MT == 1 ? EXL3_DECODE_WARPS_M8 : 8;  // warps per CTA
-  static constexpr int kStages = MT == 1 ? EXL3_DECODE_STAGES_M8 : 6;  // ring stages per warp
   static constexpr int kSeg = 256 * BITS;                    // trellis bytes per slab
+  static constexpr int kChunk = BITS <= 4 ? EXL3_DECODE_CHUNK : (EXL3_DECODE_CHUNK + 1) / 2;  // slabs per copy
+  static constexpr int kStages = MT == 1 ? EXL3_DECODE_STAGES_M8 : 3;  // ring stages (chunks) per warp
   static constexpr int kXB = 32 * 4 * MT * 2;                // x' fragment bytes per slab
-  static constexpr int kStage = kSeg;
+  static constexpr int kStage = kChunk * kSeg;
   static constexpr int kWarpRing = kStages * kStage;
   static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8;
 };
@@ -91,6 +103,13 @@ struct DecodeParams {
   int rows, y_f32, KT, smax;
   uint32_t c65536;  // 65536, opaque to the compiler (keeps the shift on the FMA pipe)
 };
+
+__device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -244,7 +263,8 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <int BITS, int MT>
-__global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_gemm_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using Cfg = DecodeCfg<BITS, MT>;
   constexpr int R = Cfg::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -253,7 +273,6 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
   const int64_t pw = (int64_t)blockIdx.x * Cfg::kWarps + warp;
   if (pw >= p.P) return;
   const int64_t z0 = pw * p.TS / p.P, z1 = (pw + 1) * p.TS / p.P;
-  const int64_t nslab = z1 - z0;
 
   uint8_t *ring = smem + warp * Cfg::kWarpRing;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kWarps * Cfg::kWarpRing) + warp * R;
@@ -265,26 +284,32 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
   }
   __syncwarp();
 
-  // Issue cursor (used by lane 0 only): next slab to stream in, as (n-block,
-  // k slab, ring stage).
+  // Issue cursor (lane 0 only): the next chunk to stream in. A chunk is up
+  // to kChunk consecutive k slabs of one n-block, fetched by one 2-D TMA copy
+  // (box: one slab row of 8 tiles x kChunk tile rows; rows past K read as 0).
+  constexpr int CHK = Cfg::kChunk;
   const int KT = p.KT;
   int i_nb = (int)(z0 / KT), i_tk = (int)(z0 % KT), i_st = 0;
+  int64_t zi = z0;
   int64_t issued = 0;
-  const int64_t slab_stride = p.tiles_n * (32 * BITS);
   auto issue_next = [&]() {
+    const int64_t left = z1 - zi;
+    const int len = (int)((KT - i_tk) < CHK ? ((int64_t)(KT - i_tk) < left ? (KT - i_tk) : left)
+                                            : (CHK < left ? CHK : left));
     const uint32_t bar = smem_u32(&bars[i_st]);
     mbar_arrive_expect_tx(bar, Cfg::kStage);
-    bulk_g2s(ring_s + i_st * Cfg::kStage, p.trellis + i_tk * slab_stride + (int64_t)i_nb * (8 * 32 * BITS),
-             Cfg::kSeg, bar);
-    if (++i_st == R) i_st = 0;
-    if (++i_tk == KT) {
+    tma_load_2d_u64(ring_s + i_st * Cfg::kStage, &tmap, bar, i_nb * (32 * BITS), i_tk);
+    zi += len;
+    i_tk += len;
+    if (i_tk == KT) {
       i_tk = 0;
       ++i_nb;
     }
+    if (++i_st == R) i_st = 0;
     ++issued;
   };
   if (lane == 0) {
-    for (int64_t t = 0; t < R - 1 && t < nslab; ++t) issue_next();
+    for (int c = 0; c < R - 1 && zi < z1; ++c) issue_next();
   }
   allow_next_grid();
   wait_prior_grid();  // x' comes from the rotation kernel
@@ -298,6 +323,7 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
   // Consumer cursor.
   int nb = (int)(z0 / KT), tk = (int)(z0 % KT), s = 0;
   uint32_t phase = 0;
+  int64_t consumed = 0;
   // x' fragments of the current slab, loaded one slab ahead.
   uint32_t bx[2 * MT], bx_next[2 * MT];
   auto load_x = [&](int k_slab, uint32_t (&dst)[2 * MT]) {
@@ -314,13 +340,14 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
     }
   };
   load_x(tk, bx_next);
-  for (int64_t t = 0; t < nslab; ++t) {
-    if (lane == 0 && issued < nslab) issue_next();
+  int64_t z = z0;
+  while (z < z1) {
+    if (lane == 0 && zi < z1) issue_next();
     if (!mbar_wait(smem_u32(&bars[s]), phase, p.status)) {
       if (lane == 0) {  // let this warp's copies in flight land before it retires
         int ws = s;
         uint32_t wp = phase;
-        for (int64_t u = t; u < issued; ++u) {
+        for (int64_t u = consumed; u < issued; ++u) {
           mbar_wait_short(smem_u32(&bars[ws]), wp);
           if (++ws == R) {
             ws = 0;
@@ -331,11 +358,16 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
       return;
     }
     const uint8_t *stage = ring + s * Cfg::kStage;
+    const int64_t left = z1 - z;
+    const int len = (int)((KT - tk) < CHK ? ((int64_t)(KT - tk) < left ? (KT - tk) : left)
+                                          : (CHK < left ? CHK : left));
+#pragma unroll 1
+    for (int i = 0; i < len; ++i) {
     uint32_t own[2 * BITS];
-    load_own_words<BITS, true>(stage + lane * 8 * BITS, own);
+    load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
 #pragma unroll
-    for (int i = 0; i < 2 * MT; ++i) bx[i] = bx_next[i];
-    if (t + 1 < nslab) load_x(tk + 1 == KT ? 0 : tk + 1, bx_next);
+    for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
+    if (z + i + 1 < z1) load_x(tk + 1 == KT ? 0 : tk + 1, bx_next);
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
     Windows<BITS> win;
     win.build(own, prev);
@@ -350,13 +382,7 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
     });
-    __syncwarp();
-    fence_proxy_async_shared();  // our reads of this stage precede its next async refill
-    if (++s == R) {
-      s = 0;
-      phase ^= 1u;
-    }
-    const bool block_done = (tk == KT - 1) || (t == nslab - 1);
+    const bool block_done = (tk == KT - 1) || (z + i == z1 - 1);
     const int cur_nb = nb;
     if (++tk == KT) {
       tk = 0;
@@ -403,6 +429,17 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1) decode_ge
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
+    }  // slabs of this chunk
+    __syncwarp();  // every lane has consumed this stage before lane 0 refills it
+#if EXL3_DECODE_PROXY_FENCE
+    fence_proxy_async_shared();
+#endif
+    if (++s == R) {
+      s = 0;
+      phase ^= 1u;
+    }
+    z += len;
+    ++consumed;
   }
 }
 
@@ -585,8 +622,15 @@ cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned 
 
 template <int BITS, int MT>
 cudaError_t launch_bits(const DecodeParams &dp, int64_t grid, cudaStream_t st) {
+  // The trellis as rows of 16-row tile strips (8-byte elements): one row is
+  // every tile of one k slab; the box is one n-block's slab x kChunk rows.
+  alignas(64) CUtensorMap tmap;
+  const uint64_t row_elems = (uint64_t)dp.tiles_n * 4 * BITS;
+  if (!encode_tensor_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, dp.trellis, row_elems, (uint64_t)dp.KT,
+                            row_elems * 8, 32 * BITS, DecodeCfg<BITS, MT>::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   return launch_dependent(decode_gemm_kernel<BITS, MT>, (unsigned)grid, DecodeCfg<BITS, MT>::kWarps * 32,
-                          DecodeCfg<BITS, MT>::kSmem, st, dp);
+                          DecodeCfg<BITS, MT>::kSmem, st, tmap, dp);
 }
 
 template <int MT>

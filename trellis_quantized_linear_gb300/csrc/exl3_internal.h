@@ -1,6 +1,7 @@
 // Host-side interfaces between the libexl3 translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -82,6 +83,10 @@ cudaError_t launch_argmax(const float *logits, int64_t M, int64_t n, int32_t *ar
                           cudaStream_t st);
 
 bool bits_supported(int bits);
+
+// 2-D TMA descriptor (row-major, dim0 contiguous), OOB reads as zero.
+bool encode_tensor_map_2d(CUtensorMap *m, CUtensorMapDataType type, const void *ptr, uint64_t dim0, uint64_t dim1,
+                          uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
 
 struct DeviceInfo;
 // The current device's cached set-up, or nullptr before exl3_init.

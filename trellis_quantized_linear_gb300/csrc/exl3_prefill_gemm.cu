@@ -323,6 +323,17 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_
 
 }  // namespace
 
+bool encode_tensor_map_2d(CUtensorMap *m, CUtensorMapDataType type, const void *ptr, uint64_t dim0, uint64_t dim1,
+                          uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)dim0, (cuuint64_t)dim1};
+  cuuint64_t strides[1] = {(cuuint64_t)stride_bytes};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, type, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t init_prefill_kernels() {
   if (!g_encode) {
     void *fn = nullptr;
