@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--quick", action="store_true", help="smaller extras (for profiling runs)")
     p.add_argument("--no-extras", action="store_true", help="headline workload only")
+    p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack",
+                   help="comma-separated sub-measurements to run after the headline")
     return p.parse_args()
 
 
@@ -592,10 +594,13 @@ def main():
     e2e = bench_e2e(args, torch, tql, dec)
     extras = {}
     if not args.no_extras and rank == 0:
+        wanted = set(args.extras.split(","))
         for name, fn in (("prefill", lambda: bench_prefill(args, torch, tql, peaks)),
                          ("crossover", lambda: bench_crossover(args, torch, tql)),
                          ("logits", lambda: bench_logits(args, torch, tql, peaks)),
                          ("mlp_stack", lambda: bench_mlp_stack(args, torch, tql))):
+            if name not in wanted:
+                continue
             try:
                 extras[name] = fn()
             except Exception as ex:  # report, never hide

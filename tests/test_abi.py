@@ -71,16 +71,19 @@ def test_workspace_holds_one_reconstruct_chunk_within_page_bound(lib):
     assert chunk == tql.EXL3_RECONSTRUCT_CHUNK_COLS
     chunk_bytes = K * chunk * g["bytes_per_weight"]
     assert chunk_bytes <= g["bound_mb"] * 1_000_000
-    # a prefill-capable workspace for a logits-width geometry holds exactly one chunk
+    # a prefill-capable workspace for a logits-width geometry holds exactly one
+    # chunk more than a decode-shaped-only one (both hold the rotated rows)
     n_gemm, M = 248192, 2048
     with_prefill = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 128, 152)
     decode_only = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 0, 152)
-    xr = M * K * 2
-    assert with_prefill - decode_only == xr + chunk_bytes
+    assert with_prefill - decode_only == chunk_bytes
     # narrower than one chunk: the scratch shrinks with n_gemm (rounded to 256 rows)
     small = tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 128, 152) - \
         tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 0, 152)
-    assert small == xr + 17408 * K * 2
+    assert small == 17408 * K * 2
+    # a pure 16-row decode workspace holds neither rotated rows nor a chunk
+    d16 = tql.exl3_linear_workspace_bytes_for(16, K, 17408, 4, 0, 152)
+    assert d16 < 32 << 20
 
 
 def _owner(z, P, TS):

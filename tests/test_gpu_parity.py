@@ -113,6 +113,31 @@ def test_linear_decode_path(oracle, K, N, bits, M):
     assert rel_err(y, ref) <= TOL
 
 
+@pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (128, 256, 1), (384, 256, 7),
+                                      (1024, 256, 2)])
+@pytest.mark.parametrize("M", [17, 100, 128, 129, 256, 300])
+def test_linear_fused_decode_path(oracle, K, N, bits, M):
+    """Decode-shaped calls above 16 rows run the fused tensor-core kernel
+    (256 rows per launch, stream-K over n-blocks and 64-row k steps)."""
+    m = synthetic.make_matrix(K, N, bits, seed=K + 7 * N + bits)
+    x = synthetic.make_activations(M, K, seed=M + 3)
+    L = Layer(m)
+    y = L.linear(to_dev(x), DECODE).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
+
+
+@pytest.mark.parametrize("M", [24, 64, 256])
+def test_fused_decode_full_gate_geometry_sampled(oracle, M):
+    K, N, bits = 5120, 17408, 4
+    m = synthetic.make_matrix(K, N, bits, seed=2)
+    x = synthetic.make_activations(M, K, seed=2)
+    y = Layer(m).linear(to_dev(x), DECODE).cpu().numpy()
+    for b in (0, 77, N // 128 - 1):
+        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
+        assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, b
+
+
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (256, 256, 1), (384, 256, 7)])
 @pytest.mark.parametrize("M", [1, 32, 130, 256])
 def test_linear_prefill_path(oracle, K, N, bits, M):

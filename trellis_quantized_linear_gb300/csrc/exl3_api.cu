@@ -45,6 +45,33 @@ exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const vo
                        uint8_t *ws, cudaStream_t st) {
   const bool prefill = m_threshold > 0 && M >= m_threshold;
   const size_t ysz = y_dtype == EXL3_F32 ? 4 : 2;
+  if (!prefill && M > kDecodeRows) {
+    // Decode-shaped with more than 16 rows: the fused tensor-core kernel,
+    // 256 rows per launch, on activations rotated once for all rows.
+    cudaError_t e = launch_hadamard128(x, ws + L.xr_off, su, M, K, dev->num_sms, st);
+    if (e != cudaSuccess) return EXL3_ERR_CUDA;
+    for (int64_t m0 = 0; m0 < M; m0 += kFusedMaxRows) {
+      FusedLaunch f;
+      f.xr = ws + L.xr_off + (size_t)(m0 * K) * 2;
+      f.xr_rows = L.xr_rows - m0;
+      f.K = K;
+      f.trellis = trellis;
+      f.bits = bits;
+      f.n_stored = n_stored;
+      f.n_gemm = n_gemm;
+      f.n_valid = n_valid;
+      f.sv = sv;
+      f.y = static_cast<uint8_t *>(y) + (size_t)(m0 * n_gemm) * ysz;
+      f.y_f32 = y_dtype == EXL3_F32;
+      f.partials = reinterpret_cast<float *>(ws + L.partials_off);
+      f.status = dev->status;
+      f.rows = (int)((M - m0) < kFusedMaxRows ? (M - m0) : kFusedMaxRows);
+      f.plan = L.fplan;
+      e = launch_fused_gemm(f, st);
+      if (e != cudaSuccess) return EXL3_ERR_CUDA;
+    }
+    return EXL3_OK;
+  }
   if (!prefill) {
     for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
       DecodeLaunch d;
@@ -131,15 +158,26 @@ bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_
   const int64_t NB = n_gemm / 128, KB = K / 128;
   L.plan = decode_plan(NB, KB, num_sms);
   size_t off = 0;
+  L.fplan = fused_plan(NB, K, num_sms);
+  L.prefill = m_threshold > 0 && M_max >= m_threshold;
+  L.fused = M_max > kDecodeRows && (m_threshold == 0 || m_threshold > kDecodeRows + 1);
   L.partials_off = off;
-  off += align_up(decode_partials_bytes(L.plan, NB), 256);
+  {
+    size_t pb = decode_partials_bytes(L.plan, NB);
+    if (L.fused) {
+      const size_t fb = fused_partials_bytes(L.fplan, NB);
+      if (fb > pb) pb = fb;
+    }
+    off += align_up(pb, 256);
+  }
   L.xf_off = off;
   off += align_up((size_t)K * 32, 256);
-  L.prefill = m_threshold > 0 && M_max >= m_threshold;
-  if (L.prefill) {
+  if (L.prefill || L.fused) {
     L.xr_rows = ceil_div(M_max, 128) * 128;
     L.xr_off = off;
     off += align_up((size_t)L.xr_rows * (size_t)K * 2, 256);
+  }
+  if (L.prefill) {
     const int64_t cols = n_gemm < EXL3_RECONSTRUCT_CHUNK_COLS ? n_gemm : EXL3_RECONSTRUCT_CHUNK_COLS;
     L.chunk_rows = ceil_div(cols, 256) * 256;
     L.wchunk_off = off;
@@ -171,7 +209,8 @@ exl3_status exl3_init(int device) {
   info.status = static_cast<int *>(status);
   if (cudaMemset(info.status, 0, sizeof(int)) != cudaSuccess) return EXL3_ERR_CUDA;
   if (init_rotate_kernels() != cudaSuccess || init_reconstruct_kernels() != cudaSuccess ||
-      init_decode_kernels() != cudaSuccess || init_prefill_kernels() != cudaSuccess)
+      init_decode_kernels() != cudaSuccess || init_prefill_kernels() != cudaSuccess ||
+      init_fused_kernels() != cudaSuccess)
     return EXL3_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return EXL3_ERR_CUDA;
   info.ready = true;

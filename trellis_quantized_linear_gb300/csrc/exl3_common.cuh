@@ -107,6 +107,66 @@ struct RowWindows {
   }
 };
 
+// Packed pair {w(state_a), w(state_b)}: both halves of each masked word are
+// summed with one fp16 add (operands selected by half), then the two sums are
+// packed. Same arithmetic as decode_pair, fewer integer-pipe instructions.
+template <bool kPackFma>
+__device__ __forceinline__ uint32_t decode_pair_sel(uint32_t state_a, uint32_t state_b) {
+  const uint32_t ua = lcg_word(state_a);
+  const uint32_t ub = lcg_word(state_b);
+  const __half2 ha = *reinterpret_cast<const __half2 *>(&ua);
+  const __half2 hb = *reinterpret_cast<const __half2 *>(&ub);
+  __half2 r;
+  if constexpr (kPackFma) {
+  // (w_a, w_a) * (1, 0) + (w_b, w_b) * (0, 1): exact, no integer-pipe op.
+  const __half2 ra = __half2half2(__hadd(__low2half(ha), __high2half(ha)));
+  const __half2 rb = __half2half2(__hadd(__low2half(hb), __high2half(hb)));
+  const __half2 one_zero = __halves2half2(__float2half_rn(1.f), __float2half_rn(0.f));
+  const __half2 zero_one = __halves2half2(__float2half_rn(0.f), __float2half_rn(1.f));
+  r = __hfma2(ra, one_zero, __hmul2(rb, zero_one));
+  } else {
+  r = __halves2half2(__hadd(__low2half(ha), __high2half(ha)), __hadd(__low2half(hb), __high2half(hb)));
+  }
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// Window states of a lane's four rows; for BITS = 4 a nibble-shifted copy
+// of the words makes every state one instruction.
+template <int BITS>
+struct Windows {
+  RowWindows<BITS> rw;
+  uint32_t X4[4 * BITS];
+  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
+    rw.build(own, prev);
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
+      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
+    }
+  }
+  template <int R, int C>
+  __device__ __forceinline__ uint32_t state() const {
+    if constexpr (BITS == 4) {
+      constexpr int s = R * 64 + (C + 1) * 4;
+      constexpr int j = s >> 4;
+      constexpr int o = s & 15;
+      static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
+      static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
+      if constexpr (o == 0) {
+        return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
+      } else if constexpr (o == 8) {
+        return __byte_perm(rw.X[j], 0u, 0x4421);
+      } else if constexpr (o == 4) {
+        return X4[j] >> 16;
+      } else {
+        return __byte_perm(X4[j], 0u, 0x4421);
+      }
+    } else {
+      return rw.template state<R, C>();
+    }
+  }
+};
+
 // Loads the 8*BITS own bytes of a thread (address 8-byte aligned for every
 // BITS, 16-byte aligned for even BITS) into 2*BITS uint32.
 template <int BITS, bool kShared>
@@ -138,6 +198,27 @@ __device__ __forceinline__ void load_own_words(const uint8_t *p, uint32_t (&own)
       own[2 * i + 1] = v.y;
     }
   }
+}
+
+// Same, from a 32-bit shared-memory address (explicit ld.shared, for buffers
+// whose generic pointer has lost its address space).
+template <int BITS>
+__device__ __forceinline__ void load_own_words_shared(uint32_t saddr, uint32_t (&own)[2 * BITS]) {
+  if constexpr ((BITS & 1) == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS / 2; ++i)
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(own[4 * i]), "=r"(own[4 * i + 1]), "=r"(own[4 * i + 2]), "=r"(own[4 * i + 3])
+                   : "r"(saddr + 16 * i));
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i)
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(own[2 * i]), "=r"(own[2 * i + 1]) : "r"(saddr + 8 * i));
+  }
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t saddr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(saddr), "r"(a), "r"(b) : "memory");
 }
 
 // The prefix word of thread (g, q) is the last own word of thread
@@ -193,6 +274,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep (up to `hint_ns`) until the phase
+// completes, so waiting warps leave their issue slots to working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for phase `parity` of an mbarrier to complete. Gives up after
 // limit_ns, records EXL3_ERR_DEVICE_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, int *status,
@@ -200,8 +295,8 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, i
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       report_timeout(status);
       return false;
     }

@@ -40,14 +40,9 @@
 #include "exl3_common.cuh"
 #include "exl3_internal.h"
 
-// Tuning knobs (compile-time): warps per CTA for <= 8 rows, and which window
-// extractions use a high-half multiply (0: none, 1: word-aligned windows,
-// 2: word-aligned and nibble-offset-4 windows) instead of integer ALU ops.
+// Tuning knobs (compile-time): warps per CTA for <= 8 rows.
 #ifndef EXL3_DECODE_WARPS_M8
 #define EXL3_DECODE_WARPS_M8 16
-#endif
-#ifndef EXL3_DECODE_MULHI_MODE
-#define EXL3_DECODE_MULHI_MODE 0
 #endif
 // Packing of two decoded fp16 weights into one mma register, per variant
 // (0: byte permute on the integer pipe; 1: multiply-add on the fp16 pipe).
@@ -101,7 +96,6 @@ struct DecodeParams {
   int *status;
   int64_t tiles_n, n_gemm, n_valid, TS, P;
   int rows, y_f32, KT, smax;
-  uint32_t c65536;  // 65536, opaque to the compiler (keeps the shift on the FMA pipe)
 };
 
 __device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
@@ -118,72 +112,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-// Packed pair {w(state_a), w(state_b)}: both halves of each masked word are
-// summed with one fp16 add (operands selected by half), then the two sums are
-// packed. Same arithmetic as decode_pair, fewer integer-pipe instructions.
-template <bool kPackFma>
-__device__ __forceinline__ uint32_t decode_pair_sel(uint32_t state_a, uint32_t state_b) {
-  const uint32_t ua = lcg_word(state_a);
-  const uint32_t ub = lcg_word(state_b);
-  const __half2 ha = *reinterpret_cast<const __half2 *>(&ua);
-  const __half2 hb = *reinterpret_cast<const __half2 *>(&ub);
-  __half2 r;
-  if constexpr (kPackFma) {
-  // (w_a, w_a) * (1, 0) + (w_b, w_b) * (0, 1): exact, no integer-pipe op.
-  const __half2 ra = __half2half2(__hadd(__low2half(ha), __high2half(ha)));
-  const __half2 rb = __half2half2(__hadd(__low2half(hb), __high2half(hb)));
-  const __half2 one_zero = __halves2half2(__float2half_rn(1.f), __float2half_rn(0.f));
-  const __half2 zero_one = __halves2half2(__float2half_rn(0.f), __float2half_rn(1.f));
-  r = __hfma2(ra, one_zero, __hmul2(rb, zero_one));
-  } else {
-  r = __halves2half2(__hadd(__low2half(ha), __high2half(ha)), __hadd(__low2half(hb), __high2half(hb)));
-  }
-  return *reinterpret_cast<const uint32_t *>(&r);
-}
-
-// Window states of a lane's four rows, for BITS = 4 with a nibble-shifted
-// copy of the words so that every state is one instruction.
-template <int BITS>
-struct Windows {
-  RowWindows<BITS> rw;
-  uint32_t X4[4 * BITS];
-  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
-    rw.build(own, prev);
-    if constexpr (BITS == 4) {
-#pragma unroll
-      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
-      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
-    }
-  }
-  // `k65536` holds 65536: a high-half product by it is the top 16 bits of a
-  // word, computed on the multiply pipe instead of the integer ALU.
-  template <int R, int C>
-  __device__ __forceinline__ uint32_t state(uint32_t k65536) const {
-    if constexpr (BITS == 4) {
-      constexpr int s = R * 64 + (C + 1) * 4;
-      constexpr int j = s >> 4;
-      constexpr int o = s & 15;
-      static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
-      static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
-      if constexpr (o == 0 && j < 4 * BITS && EXL3_DECODE_MULHI_MODE >= 1) {
-        return __umulhi(rw.X[j], k65536);  // seq[j], the top half of X[j]
-      } else if constexpr (o == 0) {
-        return rw.X[j - 1] & 0xFFFFu;      // seq[j], the low half of X[j-1]
-      } else if constexpr (o == 8) {
-        return __byte_perm(rw.X[j], 0u, 0x4421);
-      } else if constexpr (o == 4 && EXL3_DECODE_MULHI_MODE >= 2) {
-        return __umulhi(X4[j], k65536);
-      } else if constexpr (o == 4) {
-        return X4[j] >> 16;
-      } else {
-        return __byte_perm(X4[j], 0u, 0x4421);
-      }
-    } else {
-      return rw.template state<R, C>();
-    }
-  }
-};
 
 // Output rotation, sv, mask and store for the lane's values
 // v[mt][t][c] = token 8*mt + 2q + t, column nb*128 + 16g + c.
@@ -373,12 +301,11 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     win.build(own, prev);
     static_for<8>([&](auto J) {
       constexpr int j = J.value;
-      const uint32_t k = p.c65536;
       constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
-      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(k), win.template state<1, j>(k));
-      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(k), win.template state<1, j + 8>(k));
-      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(k), win.template state<3, j>(k));
-      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(k), win.template state<3, j + 8>(k));
+      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
+      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
+      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
+      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
     });
@@ -450,7 +377,7 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
 __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__restrict__ partials, int64_t smax,
                                                               int64_t slot_elems, const __half *__restrict__ sv,
                                                               void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
-                                                              int rows, int64_t P, int64_t TS, int KT) {
+                                                              int rows, int64_t P, int64_t TS, int KT, int all_blocks) {
   wait_prior_grid();  // partial slots come from the decode kernel
   const int lane = threadIdx.x & 31;
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -459,7 +386,7 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   if (nb >= n_gemm / 128) return;
   const int64_t pf = slab_owner(nb * KT, P, TS);
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
-  if (cnt == 1) return;
+  if (cnt == 1 && !all_blocks) return;  // finished by its single owner
   const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   for (int s0 = 0; s0 < cnt; s0 += 16) {
@@ -690,6 +617,15 @@ cudaError_t init_decode_kernels() {
   return init_bits<8>();
 }
 
+cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t slot_elems, const void *sv, void *y,
+                                   int y_f32, int64_t n_gemm, int64_t n_valid, int rows, int64_t P, int64_t TS,
+                                   int units_per_block, int all_blocks, cudaStream_t st) {
+  const int64_t warps = (n_gemm / 128) * rows;
+  return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st, partials, smax,
+                          slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
+                          units_per_block, all_blocks);
+}
+
 cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   const int MT = L.rows <= 8 ? 1 : 2;
   const int64_t K = L.K;
@@ -725,15 +661,12 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
   dp.y_f32 = L.y_f32;
-  dp.c65536 = 65536u;
   const int64_t grid = L.plan.grid[MT - 1];
   cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, grid, st) : launch_mt<2>(L.bits, dp, grid, st);
   if (e != cudaSuccess || dp.smax == 1) return e;
   // 3. reduce the slots of n-blocks shared by several warps
-  const int64_t warps = (L.n_gemm / 128) * L.rows;
-  return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st,
-                          (const float *)L.partials, (int64_t)dp.smax, (int64_t)8 * MT * 128, dp.sv, L.y, L.y_f32,
-                          L.n_gemm, L.n_valid, L.rows, dp.P, dp.TS, dp.KT);
+  return launch_decode_finalize(L.partials, dp.smax, (int64_t)8 * MT * 128, L.sv, L.y, L.y_f32, L.n_gemm, L.n_valid,
+                                L.rows, dp.P, dp.TS, dp.KT, /*all_blocks=*/0, st);
 }
 
 }  // namespace exl3

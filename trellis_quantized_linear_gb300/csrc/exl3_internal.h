@@ -26,9 +26,20 @@ struct DecodePlan {
 DecodePlan decode_plan(int64_t n_blocks, int64_t k_blocks, int num_sms);
 size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks);
 
+// Stream-K assignment of the fused tensor-core decode GEMM (16 < rows <= 256
+// per launch) over (128-column n-block, 64-row k step) units.
+constexpr int kFusedMaxRows = 256;
+struct FusedPlan {
+  int64_t TS = 0, P = 1, smax = 1;
+};
+FusedPlan fused_plan(int64_t n_blocks, int64_t K, int num_sms);
+size_t fused_partials_bytes(const FusedPlan &f, int64_t n_blocks);
+
 // Workspace layout shared by the size query and the calls.
 struct WorkspaceLayout {
   DecodePlan plan;
+  FusedPlan fplan;
+  bool fused = false;  // a decode-shaped call with more than 16 rows is possible
   size_t partials_off = 0, xf_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
   int64_t xr_rows = 0;      // rows of the rotated-activation buffer (multiple of 128)
   int64_t chunk_rows = 0;   // rows of the reconstruct chunk (multiple of 256)
@@ -67,7 +78,29 @@ struct PrefillLaunch {
   int num_sms;
 };
 
+struct FusedLaunch {
+  const void *xr;          // rotated rows m0.. (fp16), ld = K
+  int64_t xr_rows, K;      // rows addressable from xr (>= 1)
+  const uint16_t *trellis;
+  int bits;
+  int64_t n_stored, n_gemm, n_valid;
+  const void *sv;
+  void *y;                 // rows m0.. of y, ld = n_gemm
+  int y_f32;
+  float *partials;
+  int *status;
+  int rows;                // 17 .. 256
+  FusedPlan plan;
+};
+
 cudaError_t init_rotate_kernels();
+cudaError_t init_fused_kernels();
+cudaError_t launch_fused_gemm(const FusedLaunch &p, cudaStream_t st);
+// Sums the partial slots of shared n-blocks (slot order), output rotation,
+// sv, mask, store. Units are k slabs (decode GEMM) or k steps (fused GEMM).
+cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t slot_elems, const void *sv, void *y,
+                                   int y_f32, int64_t n_gemm, int64_t n_valid, int rows, int64_t P, int64_t TS,
+                                   int units_per_block, int all_blocks, cudaStream_t st);
 cudaError_t init_reconstruct_kernels();
 cudaError_t init_decode_kernels();
 cudaError_t init_prefill_kernels();

@@ -20,6 +20,7 @@ namespace exl3 {
 __global__ void __launch_bounds__(256) hadamard128_kernel(const __half *x, __half *y,
                                                           const __half *__restrict__ pre,
                                                           int64_t nblk, int64_t cblk, int64_t cols) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent kernel may start its prologue
   const int lane = threadIdx.x & 31;
   const int l16 = lane & 15;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
