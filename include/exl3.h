@@ -43,8 +43,9 @@
  *     graph capture: it loads every kernel and sets their attributes, so
  *     no later call loads modules, allocates or queries the device.
  *   - Supported trellis widths: bits in 1..8.
- *   - Shapes: K % 128 == 0, n_gemm % 128 == 0, n_gemm <= n_stored,
- *     n_stored % 128 == 0.
+ *   - Shapes: K % 128 == 0, K <= 131072, n_gemm % 128 == 0,
+ *     n_gemm <= n_stored, n_stored % 128 == 0, n_stored <= 2^24; others
+ *     return EXL3_ERR_INVALID_ARG.
  */
 #ifndef EXL3_H_
 #define EXL3_H_

@@ -124,8 +124,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     L = lib
     # K not a multiple of 128
     assert L.exl3_linear(good, 4, 100, good, 4, 256, 256, good, good, good, 1, 0, good, 1 << 30, None) == 1
-    # n_gemm > n_stored
+    # n_gemm > n_stored; n_stored above 2^24 columns
     assert L.exl3_linear(good, 4, 128, good, 4, 256, 384, good, good, good, 1, 0, good, 1 << 30, None) == 1
+    big = (1 << 24) + 128
+    assert L.exl3_linear(good, 4, 128, good, 4, big, 256, good, good, good, 1, 0, good, 1 << 62, None) == 1
     # bad dtype, negative threshold, negative M
     assert L.exl3_linear(good, 4, 128, good, 4, 256, 256, good, good, good, 7, 0, good, 1 << 30, None) == 1
     assert L.exl3_linear(good, 4, 128, good, 4, 256, 256, good, good, good, 1, -1, good, 1 << 30, None) == 1

@@ -33,7 +33,7 @@ bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr
 
 bool shape_ok(int64_t K, int64_t n_stored, int64_t n_gemm) {
   return K > 0 && K % 128 == 0 && K <= 131072 && n_gemm > 0 && n_gemm % 128 == 0 && n_stored % 128 == 0 &&
-         n_gemm <= n_stored;
+         n_gemm <= n_stored && n_stored <= ((int64_t)1 << 24);
 }
 
 exl3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA; }

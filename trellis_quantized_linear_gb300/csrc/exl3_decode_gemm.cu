@@ -370,39 +370,10 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
   }
 }
 
-// Sums the partial slots of every n-block shared by several warps, in slot
-// order, then applies had_r_128 over the block's 128 columns, sv and the
-// -inf mask, and writes y. One warp per (n-block, row); lane l owns columns
-// 4l .. 4l+3. N-blocks owned by a single warp were finished by that warp.
-__global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__restrict__ partials, int64_t smax,
-                                                              int64_t slot_elems, const __half *__restrict__ sv,
-                                                              void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
-                                                              int rows, int64_t P, int64_t TS, int KT, int all_blocks) {
-  wait_prior_grid();  // partial slots come from the decode kernel
-  const int lane = threadIdx.x & 31;
-  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nb = w / rows;
-  const int m = (int)(w % rows);
-  if (nb >= n_gemm / 128) return;
-  const int64_t pf = slab_owner(nb * KT, P, TS);
-  const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
-  if (cnt == 1 && !all_blocks) return;  // finished by its single owner
-  const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s0 = 0; s0 < cnt; s0 += 16) {
-    float4 f[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)  // all loads of the chunk in flight at once
-      f[i] = (s0 + i < cnt) ? __ldcg(reinterpret_cast<const float4 *>(base + (s0 + i) * slot_elems))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {  // summed in slot order
-      v[0] += f[i].x;
-      v[1] += f[i].y;
-      v[2] += f[i].z;
-      v[3] += f[i].w;
-    }
-  }
+// Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv,
+// mask and store of one row of n-block nb.
+__device__ __forceinline__ void finalize_row(float (&v)[4], const __half *__restrict__ sv, void *y, int y_f32,
+                                             int64_t n_gemm, int64_t n_valid, int64_t nb, int m, int lane) {
   {
     float a = v[0], b = v[1];
     v[0] = a + b;
@@ -440,6 +411,93 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
     *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + (int64_t)m * n_gemm + col) =
         make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
   }
+}
+
+// Sums the partial slots of every n-block shared by several warps, in slot
+// order, then applies had_r_128 over the block's 128 columns, sv and the
+// -inf mask, and writes y. One warp per (n-block, row); lane l owns columns
+// 4l .. 4l+3. N-blocks owned by a single warp were finished by that warp.
+// The decode GEMM splits an n-block over up to ~20 slots: 16 loads per lane
+// are kept in flight at once.
+__global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__restrict__ partials, int64_t smax,
+                                                              int64_t slot_elems, const __half *__restrict__ sv,
+                                                              void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
+                                                              int rows, int64_t P, int64_t TS, int KT, int all_blocks) {
+  wait_prior_grid();  // partial slots come from the decode kernel
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nb = w / rows;
+  const int m = (int)(w % rows);
+  if (nb >= n_gemm / 128) return;
+  const int64_t pf = slab_owner(nb * KT, P, TS);
+  const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
+  if (cnt == 1 && !all_blocks) return;  // finished by its single owner
+  const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0; s0 < cnt; s0 += 16) {
+    float4 f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)  // all loads of the chunk in flight at once
+      f[i] = (s0 + i < cnt) ? __ldcg(reinterpret_cast<const float4 *>(base + (s0 + i) * slot_elems))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // summed in slot order
+      v[0] += f[i].x;
+      v[1] += f[i].y;
+      v[2] += f[i].z;
+      v[3] += f[i].w;
+    }
+  }
+  finalize_row(v, sv, y, y_f32, n_gemm, n_valid, nb, m, lane);
+}
+
+// The same reduction for the fused tensor-core GEMM (up to 256 rows, 2-3
+// slots per n-block): one warp per (n-block, RPW rows) with the loads of all
+// its rows for 4 slots at a time in flight together. RPW grows with the rows
+// so that the grid keeps a few thousand warps.
+template <int RPW>
+__global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__restrict__ partials, int64_t smax,
+                                                             int64_t slot_elems, const __half *__restrict__ sv,
+                                                             void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
+                                                             int rows, int64_t P, int64_t TS, int KT) {
+  constexpr int SC = 4;
+  const int lane = threadIdx.x & 31;
+  const unsigned groups = (unsigned)((rows + RPW - 1) / RPW);
+  const unsigned w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nb = w / groups;
+  const int m0 = (int)(w % groups) * RPW;
+  if (nb >= n_gemm / 128) return;
+  const int64_t pf = slab_owner(nb * KT, P, TS);
+  const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
+  wait_prior_grid();  // partial slots come from the GEMM kernel
+  const float *base = partials + nb * smax * slot_elems + (int64_t)m0 * 128 + 4 * lane;
+  const int nr = rows - m0 < RPW ? rows - m0 : RPW;
+  float v[RPW][4];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) v[r][0] = v[r][1] = v[r][2] = v[r][3] = 0.f;
+  for (int s0 = 0; s0 < cnt; s0 += SC) {
+    float4 f[SC][RPW];
+#pragma unroll
+    for (int s = 0; s < SC; ++s)
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+        // unconditional (clamped) so that all of them are issued together
+        f[s][r] = __ldcg(reinterpret_cast<const float4 *>(base + (s0 + s < cnt ? s0 + s : cnt - 1) * slot_elems +
+                                                          (r < nr ? r : nr - 1) * 128));
+#pragma unroll
+    for (int s = 0; s < SC; ++s)  // summed in slot order
+      if (s0 + s < cnt)
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+          v[r][0] += f[s][r].x;
+          v[r][1] += f[s][r].y;
+          v[r][2] += f[s][r].z;
+          v[r][3] += f[s][r].w;
+        }
+  }
+#pragma unroll
+  for (int r = 0; r < RPW; ++r)
+    if (r < nr) finalize_row(v[r], sv, y, y_f32, n_gemm, n_valid, nb, m0 + r, lane);
 }
 
 // x' = RNE_fp16(had_r_128(x * su)) for up to 8*MT rows, in fragment order:
@@ -517,6 +575,10 @@ cudaError_t init_one() {
   cudaFuncAttributes a;
   e = cudaFuncGetAttributes(&a, decode_finalize_kernel);
   if (e != cudaSuccess) return e;
+  for (auto *k : {fused_finalize_kernel<1>, fused_finalize_kernel<2>, fused_finalize_kernel<4>}) {
+    e = cudaFuncGetAttributes(&a, k);
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncGetAttributes(&a, rotate_frag_kernel<MT>);
 }
 
@@ -532,10 +594,10 @@ cudaError_t init_bits() {
 // dependency), and the kernel itself waits before reading that kernel's
 // output.
 template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, unsigned block, size_t smem, cudaStream_t st,
                              Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -620,10 +682,17 @@ cudaError_t init_decode_kernels() {
 cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t slot_elems, const void *sv, void *y,
                                    int y_f32, int64_t n_gemm, int64_t n_valid, int rows, int64_t P, int64_t TS,
                                    int units_per_block, int all_blocks, cudaStream_t st) {
-  const int64_t warps = (n_gemm / 128) * rows;
-  return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st, partials, smax,
-                          slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
-                          units_per_block, all_blocks);
+  if (!all_blocks) {
+    const int64_t warps = (n_gemm / 128) * rows;
+    return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st, partials,
+                            smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
+                            units_per_block, all_blocks);
+  }
+  const int rpw = rows <= 64 ? 1 : rows <= 128 ? 2 : 4;
+  const unsigned grid = (unsigned)ceil_div((n_gemm / 128) * ceil_div(rows, rpw), 8);
+  auto *kern = rpw == 1 ? fused_finalize_kernel<1> : rpw == 2 ? fused_finalize_kernel<2> : fused_finalize_kernel<4>;
+  return launch_dependent(kern, grid, 256u, (size_t)0, st, partials, smax, slot_elems,
+                          static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS, units_per_block);
 }
 
 cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {

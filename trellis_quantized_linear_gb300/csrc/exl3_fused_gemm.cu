@@ -13,21 +13,27 @@
 //   y[m0:m0+M, :] = had_r_128( x'[m0:m0+M] . W ) * sv      (x' already rotated)
 //
 // Work: stream-K over (128-column n-block, 64-row k step) units, one CTA per
-// SM. Per k step:
-//   * warp 0 (one lane): TMA loads of x' (M x 64, 128-byte swizzle, one
-//     128-row tile per 128 rows);
+// SM. The decoded W^T block is the M = 128 operand of the tensor-core MMA and
+// x' the N operand, N = the rows rounded up to 32, so a few activation rows
+// cost a narrow MMA instead of a 128-row padded one. Per k step:
+//   * warp 0 (one lane): one TMA load of x' (N x 64, 128-byte swizzle);
 //   * warps 2..17 (decoders): four groups of four; group j decodes the four
 //     16-row slabs of k steps j, j+4, ...; each warp
 //     streams its slab's 8 trellis tiles through a private bulk-copy ring,
 //     decodes lane (g, q) = tile g, rows 4q..4q+3, and stores W^T into the
-//     B operand: K-major, no swizzle, 8x16-byte core matrices with strides
-//     chosen so the warp's 8-byte stores hit distinct banks;
-//   * warp 1 (one lane): tcgen05.mma M=128 N=128 K=16 per 128-row tile into a
-//     double-buffered TMEM accumulator;
+//     A operand: K-major, 128-byte swizzle (the layout the tensor core reads
+//     at full rate). Column n = 16g + c goes to operand row 16g + (c ^ g), so
+//     the eight lanes storing column step c hit eight different swizzle rows
+//     and the warp's 8-byte stores spread over all banks; the address is one
+//     XOR of a per-lane constant with a compile-time one;
+//   * warp 1 (one lane): tcgen05.mma M=128 N=npad K=16 into a double-buffered
+//     TMEM accumulator (TMEM lane = output column, TMEM column = row);
 //   * warps 18..21 (epilogue): when a CTA's part of an n-block is done they
-//     stream TMEM (one row per thread) into an fp32 partial slot; the decode
-//     finalize kernel sums each n-block's slots in slot order and applies
-//     had_r_128, sv and the -inf mask.
+//     stream TMEM (one output column per thread, the row permutation undone,
+//     32 rows per load) into an
+//     fp32 partial slot with coalesced row stores; the decode finalize kernel
+//     sums each n-block's slots in slot order and applies had_r_128, sv and
+//     the -inf mask.
 //
 // Roofline: the integer decode (K*N weights once) and the tensor work
 // (2*M*K*N) overlap; HBM traffic is the trellis (K*N*BITS/8) plus x'.
@@ -46,24 +52,33 @@ constexpr int F_BN = 128, F_BK = 64;
 constexpr int F_DEC_WARPS = 16, F_EPI_WARPS = 4;
 constexpr int F_GROUPS = F_DEC_WARPS / 4;    // k steps decoded concurrently (4 slabs each)
 constexpr int F_THREADS = (2 + F_DEC_WARPS + F_EPI_WARPS) * 32;
-constexpr int F_SB = F_GROUPS + 1, F_RD = 2;  // B stages, trellis stages per decoder warp
-constexpr int F_LBO = 144;                   // bytes between B core matrices along K
-constexpr int F_SBO = 1168;                  // bytes between B 8-row groups along N
-constexpr int F_B_STAGE = 16 * F_SBO;        // one 128 x 64 fp16 B tile with padding
-constexpr int F_A_TILE = 128 * F_BK * 2;     // one 128 x 64 fp16 x' tile (128-byte swizzle)
+constexpr int F_MAX_SA = 8;                  // x' stages at most
+constexpr int F_B_STAGE = F_BN * F_BK * 2;   // one 128 x 64 fp16 W^T tile (128-byte swizzle)
+constexpr int F_A_TILE = 128 * F_BK * 2;     // 128 rows x 64 fp16 of x' (128-byte swizzle)
 
+// MTILES = ceil(npad / 128) sizes the x' region; npad is a runtime value and
+// the region holds 32 KB / (npad * 128 B) * MTILES stages (2 .. 8).
 template <int BITS, int MTILES>
 struct FusedCfg {
-  static constexpr int kSA = MTILES == 1 ? 4 : 2;  // x' stages
   static constexpr int kSeg = 256 * BITS;
-  static constexpr int kAStage = MTILES * F_A_TILE;
-  static constexpr int kOffB = kSA * kAStage;
-  static constexpr int kOffD = kOffB + F_SB * F_B_STAGE;
-  static constexpr int kOffBar = kOffD + F_DEC_WARPS * F_RD * kSeg;
-  static constexpr int kNumBars = 2 * kSA + 2 * F_SB + 4 + 1 + F_DEC_WARPS * F_RD;
-  static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
-  static constexpr int kTmemCols = MTILES == 1 ? 256 : 512;  // 2 buffers x MTILES x 128 columns
-  static_assert(kOffB % 1024 == 0, "x' stages must stay 1024-byte aligned");
+  // Trellis bytes each decoder warp keeps in flight.
+  static constexpr int kRingBytes = 3072;
+  static constexpr int kRD = kRingBytes / kSeg < 2 ? 2 : kRingBytes / kSeg;
+  static constexpr int kARegion = 2 * MTILES * F_A_TILE;
+  // W^T stages: the decoder groups run in rounds of F_GROUPS k steps; with
+  // 2 * F_GROUPS stages a group only needs the stage the MMA was handed a
+  // whole round earlier. Take as many as shared memory holds, up to that.
+  static constexpr int kBudget = 227 * 1024 - 2048 - 2048;
+  static constexpr int kSBFit = (kBudget - kARegion - F_DEC_WARPS * kRD * kSeg) / F_B_STAGE;
+  static constexpr int kSB = kSBFit > 2 * F_GROUPS ? 2 * F_GROUPS : kSBFit;
+  static constexpr int kOffB = kARegion;
+  static constexpr int kOffD = kOffB + kSB * F_B_STAGE;
+  static constexpr int kOffBar = kOffD + F_DEC_WARPS * kRD * kSeg;
+  static constexpr int kNumBars = 2 * F_MAX_SA + 2 * kSB + 4 + 1 + F_DEC_WARPS * kRD;
+  static constexpr int kSmem = 2048 + kOffBar + kNumBars * 8 + 16;
+  static_assert(kSB > F_GROUPS, "W^T stages: one more than the k steps decoded at once, at least");
+  static_assert(kNumBars * 8 + 16 <= 2048, "barrier area");
+  static_assert(kOffB % 2048 == 0, "W^T stages must stay 2048-byte aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -75,20 +90,41 @@ struct FusedParams {
   int *status;
   int64_t tiles_n, n_gemm, n_valid, TS, P;
   int rows, y_f32, KS, smax;
+  int npad;       // MMA N: rows rounded up to 32, <= 128 * MTILES
+  int tmem_cols;  // power of two >= 2 * npad
+  int nsa;        // x' stages of npad * 128 bytes in the x' region
 };
 
 __device__ __forceinline__ int64_t unit_owner(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
 
 __device__ __forceinline__ void wait_prior_grid_f() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One lane of the (fully active) warp, the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Whole-warp bounded wait: every lane waits, and the warp agrees on the result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status)) != 0;
+}
 __device__ __forceinline__ void allow_next_grid_f() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <int BITS, int MTILES>
 __global__ void __launch_bounds__(F_THREADS, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const FusedParams p) {
   using Cfg = FusedCfg<BITS, MTILES>;
-  constexpr int F_SA = Cfg::kSA;
+  constexpr int F_SA = F_MAX_SA, F_SB = Cfg::kSB, F_RD = Cfg::kRD;
+  const int nsa = p.nsa;
+  const uint32_t a_stage = (uint32_t)p.npad * (F_BK * 2);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 2047) & ~(uintptr_t)2047);
   const uint32_t smem_s = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
   auto a_full = [&](int s) { return smem_u32(&bars[s]); };
@@ -108,7 +144,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   const int KS = p.KS;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < F_SA; ++s) {
+    for (int s = 0; s < nsa; ++s) {
       mbar_init(a_full(s), 1);
       mbar_init(a_empty(s), 1);
     }
@@ -127,7 +163,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(Cfg::kTmemCols)
+                 "r"(p.tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -137,62 +173,78 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   allow_next_grid_f();
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- x' producer ----------------
+  if (warp == 0) {
+    // ---------------- x' producer (whole warp; one elected lane issues) ----------------
     wait_prior_grid_f();  // x' comes from the rotation kernel
-    int64_t issued = 0;
+    const bool leader = elect_one();
+    int ks = (int)(zs % KS), as = 0, issued = 0;
+    uint32_t aph = 0;
     for (int kk = 0; kk < len; ++kk) {
-      const int ks = (int)((zs + kk) % KS);
-      const int as = kk % F_SA;
-      const uint32_t ua = (uint32_t)(kk / F_SA);
-      if (!mbar_wait(a_empty(as), (ua & 1u) ^ 1u, p.status)) break;
-      mbar_arrive_expect_tx(a_full(as), Cfg::kAStage);
-#pragma unroll
-      for (int mt = 0; mt < MTILES; ++mt)
-        tma_load_2d(smem_s + as * Cfg::kAStage + mt * F_A_TILE, &tmA, a_full(as), ks * F_BK, mt * 128);
+      if (!warp_wait(a_empty(as), aph ^ 1u, p.status)) break;
+      if (leader) {
+        mbar_arrive_expect_tx(a_full(as), a_stage);
+        tma_load_2d(smem_s + as * a_stage, &tmA, a_full(as), ks * F_BK, 0);
+      }
+      __syncwarp();
       ++issued;
+      if (++ks == KS) ks = 0;
+      if (++as == nsa) {
+        as = 0;
+        aph ^= 1u;
+      }
     }
-    for (int s = 0; s < F_SA; ++s) {
-      const int64_t uses = issued / F_SA + (s < issued % F_SA ? 1 : 0);
-      if (uses > 0) mbar_wait_short(a_full(s), (uint32_t)((uses - 1) & 1));
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = f16_idesc(128, F_BN);
-    int seg = 0;
-    bool ok = true;
-    for (int kk = 0; kk < len && ok; ++kk) {
-      const int ks = (int)((zs + kk) % KS);
+    if (leader)
+      for (int s = 0; s < nsa; ++s) {
+        const int uses = issued / nsa + (s < issued % nsa ? 1 : 0);
+        if (uses > 0) mbar_wait_short(a_full(s), (uint32_t)((uses - 1) & 1));
+      }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp; one elected lane issues) ----------------
+    const bool leader = elect_one();
+    const uint32_t idesc = f16_idesc(F_BN, p.npad);
+    int ks = (int)(zs % KS), seg = 0, as = 0, bs = 0;
+    uint32_t aph = 0, bph = 0;
+    for (int kk = 0; kk < len; ++kk) {
       const bool first = (kk == 0) || (ks == 0);
       const bool last = (kk == len - 1) || (ks == KS - 1);
       const int ab = seg & 1;
       if (first) {
-        if (!mbar_wait(acc_empty(ab), ((uint32_t)(seg >> 1) & 1u) ^ 1u, p.status)) break;
+        if (!warp_wait(acc_empty(ab), ((uint32_t)(seg >> 1) & 1u) ^ 1u, p.status)) break;
         tc_fence_after();
       }
-      const int as = kk % F_SA, bs = kk % F_SB;
-      if (!mbar_wait(a_full(as), (uint32_t)(kk / F_SA) & 1u, p.status)) break;
-      if (!mbar_wait(b_full(bs), (uint32_t)(kk / F_SB) & 1u, p.status)) break;
+      if (!warp_wait(a_full(as), aph, p.status)) break;
+      if (!warp_wait(b_full(bs), bph, p.status)) break;
       tc_fence_after();
-      const uint64_t bdesc = noswizzle_desc(smem_s + Cfg::kOffB + bs * F_B_STAGE, F_LBO, F_SBO);
-#pragma unroll
-      for (int mt = 0; mt < MTILES; ++mt) {
-        const uint32_t d = tmem_base + (uint32_t)((ab * MTILES + mt) * F_BN);
-        const uint64_t adesc = sw128_desc(smem_s + as * Cfg::kAStage + mt * F_A_TILE);
+      const uint64_t wdesc = sw128_desc(smem_s + Cfg::kOffB + bs * F_B_STAGE);
+      const uint64_t xdesc = sw128_desc(smem_s + as * a_stage);
+      const uint32_t d = tmem_base + (uint32_t)(ab * p.npad);
+      if (leader) {
 #pragma unroll
         for (int k16 = 0; k16 < F_BK / 16; ++k16)
-          tc_mma(d, adesc + (uint64_t)(2 * k16), bdesc + (uint64_t)((2 * F_LBO / 16) * k16), idesc,
+          tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
                  (!first || k16 > 0) ? 1u : 0u);
+        tc_commit(a_empty(as));
+        tc_commit(b_empty(bs));
+        if (last) tc_commit(acc_full(ab));
       }
-      tc_commit(a_empty(as));
-      tc_commit(b_empty(bs));
-      if (last) {
-        tc_commit(acc_full(ab));
-        ++seg;
+      __syncwarp();
+      if (last) ++seg;
+      if (++ks == KS) ks = 0;
+      if (++as == nsa) {
+        as = 0;
+        aph ^= 1u;
+      }
+      if (++bs == F_SB) {
+        bs = 0;
+        bph ^= 1u;
       }
     }
-    tc_commit(done_bar);
-    mbar_wait_short(done_bar, 0);
+    if (leader) {
+      tc_commit(done_bar);
+      mbar_wait_short(done_bar, 0);
+    }
+    __syncwarp();
   } else if (warp >= 2 && warp < 2 + F_DEC_WARPS) {
     // ---------------- decoders ----------------
     const int dw = warp - 2;
@@ -200,10 +252,23 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     const int g = lane >> 2, q = lane & 3;
     const int nmine = len > par ? (len - par + F_GROUPS - 1) / F_GROUPS : 0;
     const uint32_t ring_s = smem_s + Cfg::kOffD + dw * F_RD * Cfg::kSeg;
+    // Swizzled W^T address of (column 16g + c, rows 4q..4q+3 of slab slab_i)
+    // = (stage + lane_off) ^ (c << 7 | (c & 7) << 4), stage 2048-byte aligned:
+    // operand row t = c ^ g of
+    // 8-row atom 2g + (t >> 3), 16-byte chunk (2 slab_i + (q >> 1)) ^ (t & 7).
+    const uint32_t lane_off = (uint32_t)g * 2048u | (uint32_t)g << 7 |
+                              (((uint32_t)(2 * slab_i + (q >> 1)) ^ (uint32_t)g) & 7u) << 4 | (uint32_t)(q & 1) << 3;
     int64_t issued = 0;
+    // Cursor of the next slab to fetch (n-block, k step); fetches go in order.
+    int64_t inb = (zs + par) / KS;
+    int iks = (int)((zs + par) % KS);
     auto issue = [&](int j) {
-      const int64_t z = zs + par + (int64_t)F_GROUPS * j;
-      const int64_t nb = z / KS, tk = (z % KS) * 4 + slab_i;
+      const int64_t nb = inb, tk = (int64_t)iks * 4 + slab_i;
+      iks += F_GROUPS;
+      while (iks >= KS) {
+        iks -= KS;
+        ++inb;
+      }
       const int s = j % F_RD;
       mbar_arrive_expect_tx(dec_full(dw, s), Cfg::kSeg);
       bulk_g2s(ring_s + s * Cfg::kSeg, p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS), Cfg::kSeg,
@@ -212,6 +277,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     };
     if (lane == 0)
       for (int j = 0; j < F_RD - 1 && j < nmine; ++j) issue(j);
+    int bs = par % F_SB;  // B stage of k step par + F_GROUPS * j, and its phase
+    uint32_t bph = 0;
     for (int j = 0; j < nmine; ++j) {
       if (lane == 0 && j + F_RD - 1 < nmine) issue(j + F_RD - 1);
       const int s = j % F_RD;
@@ -225,57 +292,61 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
       Windows<BITS> win;
       win.build(own, prev);
-      const int kk = par + F_GROUPS * j;
-      const int bs = kk % F_SB;
-      if (!mbar_wait(b_empty(bs), ((uint32_t)(kk / F_SB) & 1u) ^ 1u, p.status)) break;
-      const uint32_t bt = smem_s + Cfg::kOffB + bs * F_B_STAGE + (2 * slab_i + (q >> 1)) * F_LBO + (q & 1) * 8;
+      if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) break;
+      const uint32_t bt = smem_s + Cfg::kOffB + bs * F_B_STAGE + lane_off;  // low 11 bits: lane_off's
       static_for<16>([&](auto C) {
         constexpr int cc = C.value;
+        constexpr uint32_t cx = (uint32_t)cc << 7 | (uint32_t)(cc & 7) << 4;
         const uint32_t lo = decode_pair_sel<false>(win.template state<0, cc>(), win.template state<1, cc>());
         const uint32_t hi = decode_pair_sel<false>(win.template state<2, cc>(), win.template state<3, cc>());
-        const int n = 16 * g + cc;
-        st_shared_v2(bt + (n >> 3) * F_SBO + (n & 7) * 16, lo, hi);
+        st_shared_v2(bt ^ cx, lo, hi);
       });
       fence_proxy_async_shared();  // make the generic stores visible to the tensor core
       __syncwarp();
       if (lane == 0) mbar_arrive(b_full(bs));
+      bs += F_GROUPS;
+      if (bs >= F_SB) {
+        bs -= F_SB;
+        bph ^= 1u;
+      }
     }
   } else if (warp >= 2 + F_DEC_WARPS) {
     // ---------------- epilogue ----------------
     wait_prior_grid_f();  // the previous kernel may still read the partial slots
     const int lg = warp & 3;
     int seg = 0;
-    for (int kk = 0; kk < len; ++kk) {
-      const int64_t z = zs + kk;
-      const int ks = (int)(z % KS);
-      if (!((kk == len - 1) || (ks == KS - 1))) continue;
-      const int64_t nb = z / KS;
+    int64_t nb = zs / KS;
+    // Segment ends (local k step indexes): the last k step of each n-block
+    // the range touches, or the range's last k step.
+    for (int e = (int)(KS - 1 - zs % KS);; e += KS, ++nb) {
       const int ab = seg & 1;
       if (!mbar_wait(acc_full(ab), (uint32_t)(seg >> 1) & 1u, p.status)) break;
       tc_fence_after();
       // Every CTA stores its part of the n-block as an fp32 partial slot; the
       // finalize kernel sums the slots and applies the output rotation.
       const int64_t pf = unit_owner(nb * KS, p.P, p.TS);
-      float *slot = p.partials + (nb * p.smax + (c - pf)) * (int64_t)(MTILES * 128 * 128);
+      const int i = lg * 32 + lane;  // operand row = TMEM lane
+      float *slot = p.partials + (nb * p.smax + (c - pf)) * (int64_t)(MTILES * 128 * 128) + 16 * (i >> 4) +
+                    ((i & 15) ^ (i >> 4));
+      const uint32_t taddr = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(ab * p.npad);
 #pragma unroll 1
-      for (int mt = 0; mt < MTILES; ++mt) {
-        const int m = mt * 128 + lg * 32 + lane;
-        const uint32_t taddr = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)((ab * MTILES + mt) * F_BN);
-#pragma unroll 1
-        for (int j4 = 0; j4 < 4; ++j4) {
-          float t[32];
-          tmem_ld32(taddr + 32 * j4, t);
-          if (m < p.rows) {
-            float4 *dst = reinterpret_cast<float4 *>(slot + (int64_t)m * 128 + 32 * j4);
+      for (int m0 = 0; m0 < p.rows; m0 += 32) {
+        float t[32];
+        tmem_ld32(taddr + m0, t);
+        if (m0 + 32 <= p.rows) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a) dst[a] = make_float4(t[4 * a], t[4 * a + 1], t[4 * a + 2], t[4 * a + 3]);
-          }
+          for (int r = 0; r < 32; ++r) slot[(int64_t)(m0 + r) * 128] = t[r];
+        } else {
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (m0 + r < p.rows) slot[(int64_t)(m0 + r) * 128] = t[r];
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(ab));
       ++seg;
+      if (e >= len - 1) break;
     }
   }
 
@@ -283,7 +354,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(Cfg::kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
                  : "memory");
   }
 }
@@ -365,10 +436,14 @@ cudaError_t init_fused_kernels() {
 }
 
 cudaError_t launch_fused_gemm(const FusedLaunch &L, cudaStream_t st) {
-  const int MTILES = L.rows <= 128 ? 1 : 2;
+  if (L.rows < 1 || L.rows > kFusedMaxRows) return cudaErrorInvalidValue;
+  const int npad = (L.rows + 31) & ~31;
+  const int MTILES = npad <= 128 ? 1 : 2;
+  int tmem_cols = 32;
+  while (tmem_cols < 2 * npad) tmem_cols *= 2;
   alignas(64) CUtensorMap tmA;
   if (!encode_tensor_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.xr, (uint64_t)L.K, (uint64_t)L.xr_rows,
-                            (uint64_t)L.K * 2, F_BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                            (uint64_t)L.K * 2, F_BK, (uint32_t)npad, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   FusedParams fp;
   fp.trellis = reinterpret_cast<const uint8_t *>(L.trellis);
@@ -385,6 +460,10 @@ cudaError_t launch_fused_gemm(const FusedLaunch &L, cudaStream_t st) {
   fp.y_f32 = L.y_f32;
   fp.KS = (int)(L.K / F_BK);
   fp.smax = (int)L.plan.smax;
+  fp.npad = npad;
+  fp.tmem_cols = tmem_cols;
+  fp.nsa = (2 * MTILES * F_A_TILE) / (npad * F_BK * 2);
+  if (fp.nsa > F_MAX_SA) fp.nsa = F_MAX_SA;
   cudaError_t e = MTILES == 1 ? launch_mt<1>(L.bits, tmA, fp, fp.P, st) : launch_mt<2>(L.bits, tmA, fp, fp.P, st);
   if (e != cudaSuccess) return e;
   return launch_decode_finalize(L.partials, fp.smax, (int64_t)MTILES * 128 * 128, L.sv, L.y, L.y_f32, L.n_gemm,
