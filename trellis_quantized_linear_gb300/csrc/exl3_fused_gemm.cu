@@ -193,11 +193,12 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         aph ^= 1u;
       }
     }
+    // Before leaving (also after a timeout), wait for the loads that may still
+    // be in flight, in issue order: load u was issued only after load u - nsa
+    // had been consumed, so at most the last nsa can be outstanding.
     if (leader)
-      for (int s = 0; s < nsa; ++s) {
-        const int uses = issued / nsa + (s < issued % nsa ? 1 : 0);
-        if (uses > 0) mbar_wait_short(a_full(s), (uint32_t)((uses - 1) & 1));
-      }
+      for (int u = issued > nsa ? issued - nsa : 0; u < issued; ++u)
+        mbar_wait_short(a_full(u % nsa), (uint32_t)(u / nsa) & 1u);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp; one elected lane issues) ----------------
@@ -279,12 +280,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       for (int j = 0; j < F_RD - 1 && j < nmine; ++j) issue(j);
     int bs = par % F_SB;  // B stage of k step par + F_GROUPS * j, and its phase
     uint32_t bph = 0;
+    // On a timeout the warp stops, but first waits (bounded) for the copies
+    // it still has in flight into its ring, in issue order.
+    auto drain_from = [&](int64_t u0) {
+      if (lane == 0)
+        for (int64_t u = u0; u < issued; ++u) mbar_wait_short(dec_full(dw, (int)(u % F_RD)), (uint32_t)(u / F_RD) & 1u);
+    };
     for (int j = 0; j < nmine; ++j) {
       if (lane == 0 && j + F_RD - 1 < nmine) issue(j + F_RD - 1);
       const int s = j % F_RD;
       if (!mbar_wait(dec_full(dw, s), (uint32_t)(j / F_RD) & 1u, p.status)) {
-        if (lane == 0)
-          for (int64_t u = j; u < issued; ++u) mbar_wait_short(dec_full(dw, (int)(u % F_RD)), (uint32_t)(u / F_RD) & 1u);
+        drain_from(j);
         break;
       }
       uint32_t own[2 * BITS];
@@ -292,7 +298,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
       Windows<BITS> win;
       win.build(own, prev);
-      if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) break;
+      if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) {
+        drain_from(j + 1);
+        break;
+      }
       const uint32_t bt = smem_s + Cfg::kOffB + bs * F_B_STAGE + lane_off;  // low 11 bits: lane_off's
       static_for<16>([&](auto C) {
         constexpr int cc = C.value;
