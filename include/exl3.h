@@ -169,12 +169,16 @@ exl3_status exl3_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64
  *   m_threshold: path choice made inside this call on its own M ([P1]
  *          "Change": the dispatch must live inside the op, not in a branch
  *          a tracer can freeze). M < m_threshold, or m_threshold == 0,
- *          takes the decode-shaped path: one fused kernel per 16 rows that
- *          rotates x, decodes the trellis inside the GEMM and finishes with
- *          the output rotation. Otherwise the prefill-shaped path runs
- *          had_r_128 -> reconstruct (32768-column chunks into the workspace)
- *          -> tensor-core GEMM with the output rotation fused in its
- *          epilogue.
+ *          takes the decode-shaped path, where the trellis is decoded
+ *          inside the GEMM and never materialised: for M <= 16 a stream-K
+ *          kernel with the decoded weights as the mma.sync operand; for
+ *          larger M one tensor-core (tcgen05) kernel per 256 rows whose
+ *          producer warps decode straight into the MMA operand buffers.
+ *          Otherwise the prefill-shaped path runs had_r_128 -> reconstruct
+ *          (32768-column chunks into the workspace) -> tensor-core GEMM with
+ *          the output rotation fused in its epilogue. On one GB300 the
+ *          prefill-shaped path becomes faster between M = 384 and M = 1024
+ *          depending on the shape (both 4-bit MLP shapes measured).
  *   workspace: device buffer of at least
  *          exl3_linear_workspace_bytes(M, K, n_gemm, bits, m_threshold)
  *          bytes, cleared once by exl3_workspace_init. Calls that share a

@@ -114,11 +114,13 @@ def test_linear_decode_path(oracle, K, N, bits, M):
 
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (128, 256, 1), (384, 256, 7),
-                                      (1024, 256, 2)])
-@pytest.mark.parametrize("M", [17, 100, 128, 129, 256, 300])
+                                      (1024, 256, 2), (256, 384, 5), (384, 256, 8)])
+@pytest.mark.parametrize("M", [17, 50, 100, 128, 129, 200, 256, 300])
 def test_linear_fused_decode_path(oracle, K, N, bits, M):
     """Decode-shaped calls above 16 rows run the fused tensor-core kernel
-    (256 rows per launch, stream-K over n-blocks and 64-row k steps)."""
+    (256 rows per launch, stream-K over n-blocks and 64-row k steps). The M
+    values cover MMA widths 32..256 and x' rings of 8, 4, 3 and 2 stages;
+    M = 300 is a 256-row launch plus a 44-row one."""
     m = synthetic.make_matrix(K, N, bits, seed=K + 7 * N + bits)
     x = synthetic.make_activations(M, K, seed=M + 3)
     L = Layer(m)
