@@ -202,43 +202,135 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp; one elected lane issues) ----------------
+    // With 3 or more x' stages, each round the warp tests, without blocking,
+    // whether the next `look` k steps' W^T stages (lanes 0..3) and x' stages
+    // (lanes 8..11) are full and issues every consecutive ready k step in
+    // one batch: a satisfied
+    // barrier costs one test per batch, not a wait per k step. The lookahead
+    // stays below both ring sizes, so each tested stage's previous use is
+    // already consumed and its next use cannot complete before this warp
+    // frees it: the parity tests cannot alias. Only when the current k step
+    // is not ready does the warp block (bounded) on it. A batch ends where
+    // an n-block ends, so each accumulator hand-off stays per segment.
     const bool leader = elect_one();
     const uint32_t idesc = f16_idesc(F_BN, p.npad);
     int ks = (int)(zs % KS), seg = 0, as = 0, bs = 0;
     uint32_t aph = 0, bph = 0;
-    for (int kk = 0; kk < len; ++kk) {
-      const bool first = (kk == 0) || (ks == 0);
-      const bool last = (kk == len - 1) || (ks == KS - 1);
-      const int ab = seg & 1;
-      if (first) {
-        if (!warp_wait(acc_empty(ab), ((uint32_t)(seg >> 1) & 1u) ^ 1u, p.status)) break;
+    if (nsa < 3) {
+      // Two x' stages (wide x' tiles): the next step's x' cannot land before
+      // this warp frees a stage, so batches cannot form; one k step at a time.
+      for (int kk = 0; kk < len; ++kk) {
+        const bool first = (kk == 0) || (ks == 0);
+        const bool last = (kk == len - 1) || (ks == KS - 1);
+        const int ab = seg & 1;
+        if (first) {
+          if (!warp_wait(acc_empty(ab), ((uint32_t)(seg >> 1) & 1u) ^ 1u, p.status)) break;
+          tc_fence_after();
+        }
+        if (!warp_wait(a_full(as), aph, p.status)) break;
+        if (!warp_wait(b_full(bs), bph, p.status)) break;
         tc_fence_after();
-      }
-      if (!warp_wait(a_full(as), aph, p.status)) break;
-      if (!warp_wait(b_full(bs), bph, p.status)) break;
-      tc_fence_after();
-      const uint64_t wdesc = sw128_desc(smem_s + Cfg::kOffB + bs * F_B_STAGE);
-      const uint64_t xdesc = sw128_desc(smem_s + as * a_stage);
-      const uint32_t d = tmem_base + (uint32_t)(ab * p.npad);
-      if (leader) {
+        const uint64_t wdesc = sw128_desc(smem_s + Cfg::kOffB + bs * F_B_STAGE);
+        const uint64_t xdesc = sw128_desc(smem_s + as * a_stage);
+        const uint32_t d = tmem_base + (uint32_t)(ab * p.npad);
+        if (leader) {
 #pragma unroll
-        for (int k16 = 0; k16 < F_BK / 16; ++k16)
-          tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
-                 (!first || k16 > 0) ? 1u : 0u);
-        tc_commit(a_empty(as));
-        tc_commit(b_empty(bs));
-        if (last) tc_commit(acc_full(ab));
+          for (int k16 = 0; k16 < F_BK / 16; ++k16)
+            tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
+                   (!first || k16 > 0) ? 1u : 0u);
+          tc_commit(a_empty(as));
+          tc_commit(b_empty(bs));
+          if (last) tc_commit(acc_full(ab));
+        }
+        __syncwarp();
+        if (last) ++seg;
+        if (++ks == KS) ks = 0;
+        if (++as == nsa) {
+          as = 0;
+          aph ^= 1u;
+        }
+        if (++bs == F_SB) {
+          bs = 0;
+          bph ^= 1u;
+        }
       }
-      __syncwarp();
-      if (last) ++seg;
-      if (++ks == KS) ks = 0;
-      if (++as == nsa) {
-        as = 0;
-        aph ^= 1u;
-      }
-      if (++bs == F_SB) {
-        bs = 0;
-        bph ^= 1u;
+    } else {
+      const int look = nsa < 4 ? nsa : 4;  // F_SB > 4 always
+      for (int kk = 0; kk < len;) {
+        const int ab = seg & 1;
+        if (kk == 0 || ks == 0) {
+          if (!warp_wait(acc_empty(ab), ((uint32_t)(seg >> 1) & 1u) ^ 1u, p.status)) break;
+          tc_fence_after();
+        }
+        bool rdy = false;
+        {
+          const int j = lane & 7;
+          if (lane < 16 && j < look && kk + j < len) {
+            if (lane < 8) {
+              int s = bs + j;
+              uint32_t ph = bph;
+              if (s >= F_SB) {
+                s -= F_SB;
+                ph ^= 1u;
+              }
+              rdy = mbar_test_wait(b_full(s), ph);
+            } else {
+              int s = as + j;
+              uint32_t ph = aph;
+              if (s >= nsa) {
+                s -= nsa;
+                ph ^= 1u;
+              }
+              rdy = mbar_test_wait(a_full(s), ph);
+            }
+          }
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, rdy);
+        __syncwarp();  // the lanes' acquires are ordered before the issuing lane's MMAs
+        const uint32_t both = bal & (bal >> 8) & 0xFFu;
+        int n = __ffs(~both) - 1;  // leading run of ready k steps
+        if (n > KS - ks) n = KS - ks;
+        if (n == 0) {
+          if (!warp_wait(a_full(as), aph, p.status)) break;
+          if (!warp_wait(b_full(bs), bph, p.status)) break;
+          n = 1;
+        }
+        tc_fence_after();
+        if (leader) {
+          int a = as, b = bs, k2 = ks;
+          const uint32_t d = tmem_base + (uint32_t)(ab * p.npad);
+          for (int t = 0; t < n; ++t) {
+            const bool first = (kk + t == 0) || (k2 == 0);
+            const bool last = (kk + t == len - 1) || (k2 == KS - 1);
+            const uint64_t wdesc = sw128_desc(smem_s + Cfg::kOffB + b * F_B_STAGE);
+            const uint64_t xdesc = sw128_desc(smem_s + a * a_stage);
+#pragma unroll
+            for (int k16 = 0; k16 < F_BK / 16; ++k16)
+              tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
+                     (!first || k16 > 0) ? 1u : 0u);
+            tc_commit(a_empty(a));
+            tc_commit(b_empty(b));
+            if (last) tc_commit(acc_full(ab));
+            if (++a == nsa) a = 0;
+            if (++b == F_SB) b = 0;
+            if (++k2 == KS) k2 = 0;
+          }
+        }
+        __syncwarp();
+        const int kl = kk + n - 1, ksl = ks + n - 1;  // the batch's last k step (ksl < KS)
+        if (kl == len - 1 || ksl == KS - 1) ++seg;
+        kk += n;
+        ks = ksl + 1 == KS ? 0 : ksl + 1;
+        as += n;
+        if (as >= nsa) {
+          as -= nsa;
+          aph ^= 1u;
+        }
+        bs += n;
+        if (bs >= F_SB) {
+          bs -= F_SB;
+          bph ^= 1u;
+        }
       }
     }
     if (leader) {
