@@ -14,7 +14,9 @@ Also measured in the same run (reported as sub-objects of the JSON line):
   crossover - both paths timed at M in {64 .. 4096} on both MLP geometries;
   logits    - the odd-vocab masked logits call at M in {1, 16, 2048};
   mlp_stack - 64 dense MLP layers (gate, up, SiLU*up, down) at M=2048,
-              bits 4 and 3: ms per pass and the reconstruct/GEMM split.
+              bits 4 and 3: ms per pass and the reconstruct/GEMM split;
+  decode_stack - the same 64-layer stack as one decode step at M = 1 and
+              16 (bits 4), run eagerly and as one captured CUDA graph.
 
 --impl reference times the CPU oracle (test infrastructure) on the host's
 cores on a bounded sample of the same workload, as the reference arm.
@@ -61,7 +63,7 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--quick", action="store_true", help="smaller extras (for profiling runs)")
     p.add_argument("--no-extras", action="store_true", help="headline workload only")
-    p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack",
+    p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack,decode_stack",
                    help="comma-separated sub-measurements to run after the headline")
     return p.parse_args()
 
@@ -322,7 +324,9 @@ def bench_decode(args, torch, tql, peaks, dist):
                                                  "decode_gemm_gate_k5120_n17408_b4.md"),
                      "peak_kind": f"of {peaks['source']} (burst copy)", "kernel": "decode_gemm_kernel<4,*>",
                      "bytes_per_launch": wbytes},
-        "gpu_launches": args.steps * len(Ms),
+        # each decode-shaped call launches three kernels: input rotation,
+        # decode GEMM, slot reduction
+        "gpu_launches": args.steps * len(Ms) * 3,
         "weights_per_step_bytes": per_step_bytes,
         "mats": mats, "xs": xs, "ws": ws,
     }
@@ -513,6 +517,65 @@ def bench_mlp_stack(args, torch, tql):
     return out
 
 
+def bench_decode_stack(args, torch, tql, peaks):
+    """One decode step of the 64-layer MLP stack (gate, up 5120->17408;
+    SiLU(gate)*up; down 17408->5120; bits 4) at M = 1 and 16: 192 linear
+    calls and 64 glue calls, timed eagerly (one host launch per kernel) and
+    replayed as one captured CUDA graph. Weights (8.56 GB) are drawn on the
+    device (timing only); every weight byte comes from HBM once per step."""
+    st = synthetic.MLP_STACK
+    L, d, f, bits = st["layers"], st["d_model"], st["d_ff"], 4
+    if args.quick:
+        L = 8
+    layers = []
+    for l in range(L):
+        mats = []
+        for j, (K, N) in enumerate(((d, f), (d, f), (f, d))):
+            tr, su, sv = synthetic.make_matrix_device(K, N, bits, seed=st["seed_base"] + l, matrix_index=j)
+            mats.append(dict(K=K, N=N, tr=tr, su=su, sv=sv))
+        layers.append(mats)
+    wbytes = sum(m["tr"].numel() * 2 for lay in layers for m in lay)
+    Mmax = 16
+    ws = torch.empty(max(tql.exl3_linear_workspace_bytes(Mmax, d, f, bits, 0),
+                         tql.exl3_linear_workspace_bytes(Mmax, f, d, bits, 0)), dtype=torch.uint8, device="cuda")
+    tql.exl3_workspace_init(ws)
+    out = {"layers": L, "bits": bits, "trellis_gb": round(wbytes / 1e9, 2)}
+    stream = torch.cuda.Stream()
+    for M in (1, 16):
+        x0 = _dev(torch, synthetic.make_activations(M, d, seed=st["seed_base"], x_scale=0.05))
+        g = torch.empty((M, f), dtype=torch.float16, device="cuda")
+        u = torch.empty_like(g)
+        h = torch.empty_like(g)
+        xa = torch.empty((M, d), dtype=torch.float16, device="cuda")
+
+        def one_step():
+            xin = x0
+            for mg, mu, md in layers:
+                for m, yout in ((mg, g), (mu, u)):
+                    tql.exl3_linear(xin, M, m["K"], m["tr"], bits, m["N"], m["N"], m["su"], m["sv"], yout,
+                                    tql.EXL3_F16, 0, ws)
+                tql.exl3_silu_mul(g, u, h)
+                tql.exl3_linear(h, M, md["K"], md["tr"], bits, md["N"], md["N"], md["su"], md["sv"], xa,
+                                tql.EXL3_F16, 0, ws)
+                xin = xa
+
+        with torch.cuda.stream(stream):
+            eager_ms = time_fn(torch, one_step, 5, 2)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                one_step()
+            graph_ms = time_fn(torch, gr.replay, 20, 3)
+        out[f"M{M}"] = {"eager_ms": round(eager_ms, 3), "graph_ms": round(graph_ms, 3),
+                        "graph_speedup": round(eager_ms / graph_ms, 3),
+                        "graph_weight_gbs": round(wbytes / (graph_ms * 1e-3) / 1e9, 1),
+                        "graph_frac_hbm": round(wbytes / (graph_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                        "us_per_linear": round(graph_ms * 1e3 / (3 * L), 2)}
+        del gr
+    del layers, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle: baseline leg and reference arm
 # ---------------------------------------------------------------------------
@@ -598,7 +661,8 @@ def main():
         for name, fn in (("prefill", lambda: bench_prefill(args, torch, tql, peaks)),
                          ("crossover", lambda: bench_crossover(args, torch, tql)),
                          ("logits", lambda: bench_logits(args, torch, tql, peaks)),
-                         ("mlp_stack", lambda: bench_mlp_stack(args, torch, tql))):
+                         ("mlp_stack", lambda: bench_mlp_stack(args, torch, tql)),
+                         ("decode_stack", lambda: bench_decode_stack(args, torch, tql, peaks))):
             if name not in wanted:
                 continue
             try:

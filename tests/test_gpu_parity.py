@@ -377,6 +377,62 @@ def test_graph_capture_keeps_each_path(oracle):
     assert rel_err(y_big.cpu().numpy(), ref_b) <= TOL
 
 
+@pytest.mark.parametrize("M", [1, 16, 40])
+def test_decode_stack_graph_matches_eager(oracle, M):
+    """A whole decode step of a small MLP stack (3 layers of gate, up,
+    SiLU*up, down) captured as one CUDA graph gives the eager result bit for
+    bit (same kernels, deterministic reductions), and its first gate output
+    matches the oracle."""
+    torch = torch_mod()
+    d, f, bits, nl = 256, 384, 4, 3
+    layers = []
+    for l in range(nl):
+        mats = [synthetic.make_matrix(K, N, bits, seed=100 + 3 * l + j) for j, (K, N) in
+                enumerate(((d, f), (d, f), (f, d)))]
+        layers.append([Layer(m) for m in mats])
+    ws = torch.zeros(max(tql.exl3_linear_workspace_bytes(M, d, f, bits, 0),
+                         tql.exl3_linear_workspace_bytes(M, f, d, bits, 0)), dtype=torch.uint8, device="cuda")
+    tql.exl3_workspace_init(ws)
+    x = synthetic.make_activations(M, d, seed=77, x_scale=0.5)
+    x0 = to_dev(x)
+    g = torch.empty((M, f), dtype=torch.float16, device="cuda")
+    u, h = torch.empty_like(g), torch.empty_like(g)
+    xa = torch.empty((M, d), dtype=torch.float16, device="cuda")
+    g1 = torch.empty((M, f), dtype=torch.float32, device="cuda")
+
+    def step():
+        xin = x0
+        for li, (lg, lu, ld) in enumerate(layers):
+            if li == 0:
+                tql.exl3_linear(xin, M, d, lg.trellis, bits, f, f, lg.su, lg.sv, g1, tql.EXL3_F32, 0, ws)
+            tql.exl3_linear(xin, M, d, lg.trellis, bits, f, f, lg.su, lg.sv, g, tql.EXL3_F16, 0, ws)
+            tql.exl3_linear(xin, M, d, lu.trellis, bits, f, f, lu.su, lu.sv, u, tql.EXL3_F16, 0, ws)
+            tql.exl3_silu_mul(g, u, h)
+            tql.exl3_linear(h, M, f, ld.trellis, bits, d, d, ld.su, ld.sv, xa, tql.EXL3_F16, 0, ws)
+            xin = xa
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager_out, eager_g1 = xa.clone(), g1.clone()
+    xa.fill_(0)
+    g1.fill_(0)
+    with torch.cuda.stream(s):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            step()
+    xa.fill_(0)
+    torch.cuda.synchronize()
+    gr.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(xa.view(torch.int16), eager_out.view(torch.int16))
+    assert torch.equal(g1.view(torch.int32), eager_g1.view(torch.int32))
+    m0 = layers[0][0].m
+    ref = oracle.linear(x, m0.trellis, bits, d, f, m0.su, m0.sv)
+    assert rel_err(g1.cpu().numpy(), ref) <= TOL
+
+
 # ---------------------------------------------------------------------------
 # failure detection without a fault: a bounded wait that runs out
 # ---------------------------------------------------------------------------
