@@ -62,6 +62,9 @@ def _load():
             getattr(lib, name).restype = None
         lib.oracle_reconstruct.argtypes = [_u16p, ctypes.c_int, _i64, _i64, _i64, _i64, _u16p]
         lib.oracle_reconstruct.restype = None
+        lib.oracle_reconstruct_rotated.argtypes = [_u16p, ctypes.c_int, _i64, _i64, _u16p, _u16p, _i64, _i64,
+                                                   ctypes.c_int, _u16p]
+        lib.oracle_reconstruct_rotated.restype = ctypes.c_int
         lib.oracle_hadamard128_f64.argtypes = [_f64p, _f64p, _i64]
         lib.oracle_hadamard128_f64.restype = None
         lib.oracle_hadamard128_f32.argtypes = [_f32p, _f32p, _i64]
@@ -146,6 +149,28 @@ def reconstruct(trellis, bits: int, K: int, n_stored: int, n0: int = 0, ncols: i
     out = np.zeros((K, ncols), np.uint16)
     _load().oracle_reconstruct(_bits16(trellis), int(bits), K, n_stored, n0, ncols, out)
     return out.view(np.float16)
+
+
+def reconstruct_rotated(trellis, bits: int, K: int, n_stored: int, su, sv, n0: int = 0,
+                        ncols: int | None = None, layout: int = 0) -> np.ndarray:
+    """Columns [n0, n0+ncols) of the weight-side rotated weight
+    W' = diag(su) . had_r_128(K) . W . had_r_128(N) . diag(sv) as float16,
+    K x ncols (layout 0) or ncols x K (layout 1)."""
+    if ncols is None:
+        ncols = n_stored - n0
+    shape = (K, ncols) if layout == 0 else (ncols, K)
+    out = np.zeros(shape, np.uint16)
+    rc = _load().oracle_reconstruct_rotated(_bits16(trellis), int(bits), K, n_stored, _bits16(su), _bits16(sv),
+                                            n0, ncols, int(layout), out)
+    if rc != 0:
+        raise ValueError(f"oracle_reconstruct_rotated rejected its arguments (rc={rc})")
+    return out.view(np.float16)
+
+
+def matmul_f64(x, w) -> np.ndarray:
+    """x . w in fp64 for fp16 x (M x K) and fp16 w (K x n): the weight-side
+    variant's layer output from its rotated weight."""
+    return np.asarray(x, np.float16).astype(np.float64) @ np.asarray(w, np.float16).astype(np.float64)
 
 
 def hadamard128_f64(v) -> np.ndarray:

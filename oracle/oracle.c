@@ -269,6 +269,65 @@ void oracle_input_rotation(const uint16_t *x, const uint16_t *su, int64_t rows, 
     }
 }
 
+/*
+ * Weight-side rotation variant: columns [n0, n0+ncols) of
+ *     W' = diag(su) . had_r_128(K) . W . had_r_128(N) . diag(sv)
+ * (the rotations of the linear layer moved onto the weight, so that
+ * x . W' = had_r_128(had_r_128(x * su) . W) * sv in exact arithmetic; the
+ * "reconstruct_had_slice" of vLLM PR #316, section "Kernel measurements").
+ * The pages do not give its arithmetic; this library defines it per
+ * 128 x 128 block of W as:
+ *   1. t = fp32(w);
+ *   2. fast WHT of every column along k, fp32, stages h = 1, 2, ..., 64;
+ *   3. t = t * fp32(su[k])                      (fp32 product);
+ *   4. fast WHT of every row along n, same stages;
+ *   5. t = t * 2^-7                              (exact: the two 1/sqrt(128));
+ *   6. t = t * fp32(sv[n])                      (fp32 product);
+ *   7. RNE to fp16.
+ * layout 0: out is K x ncols (ld ncols); layout 1: ncols x K (ld K).
+ */
+int oracle_reconstruct_rotated(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored,
+                               const uint16_t *su, const uint16_t *sv, int64_t n0, int64_t ncols,
+                               int layout, uint16_t *out)
+{
+    if (K % 128 || n0 % 128 || ncols % 128 || n0 + ncols > n_stored || bits < 1 || bits > 8 ||
+        (layout != 0 && layout != 1))
+        return -1;
+    uint16_t *w = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K * ncols));
+    if (!w) return -2;
+    oracle_reconstruct(trellis, bits, K, n_stored, n0, ncols, w);
+    int64_t nkb = K / 128, nnb = ncols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t blk = 0; blk < nkb * nnb; ++blk) {
+        int64_t kb = blk / nnb, nb = blk % nnb;
+        float *t = (float *)malloc(sizeof(float) * 128 * 128);
+        float col[128];
+        for (int i = 0; i < 128; ++i)
+            for (int j = 0; j < 128; ++j)
+                t[i * 128 + j] = oracle_half_to_float(w[(kb * 128 + i) * ncols + nb * 128 + j]);
+        for (int j = 0; j < 128; ++j) {
+            for (int i = 0; i < 128; ++i) col[i] = t[i * 128 + j];
+            fwht128_f32(col);
+            for (int i = 0; i < 128; ++i) t[i * 128 + j] = col[i];
+        }
+        for (int i = 0; i < 128; ++i) {
+            float s = oracle_half_to_float(su[kb * 128 + i]);
+            for (int j = 0; j < 128; ++j) t[i * 128 + j] = t[i * 128 + j] * s;
+            fwht128_f32(t + i * 128);
+        }
+        for (int i = 0; i < 128; ++i)
+            for (int j = 0; j < 128; ++j) {
+                float v = t[i * 128 + j] * 0.0078125f;
+                v = v * oracle_half_to_float(sv[n0 + nb * 128 + j]);
+                int64_t k = kb * 128 + i, n = nb * 128 + j;
+                out[layout == 0 ? k * ncols + n : n * K + k] = oracle_float_to_half_rne(v);
+            }
+        free(t);
+    }
+    free(w);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Linear layer                                                               */
 /* ------------------------------------------------------------------------ */

@@ -266,6 +266,65 @@ def test_linear_column_slices_agree(oracle):
     assert np.array_equal(full[:, 256:384], part)
 
 
+# --------------------------------------------------------------------------
+# Weight-side rotation variant
+# --------------------------------------------------------------------------
+
+def _dense_rotated_weight(oracle, m, K, N, bits):
+    """diag(su) . H_K . W . H_N . diag(sv) in fp64 with scipy's Sylvester H."""
+    W = oracle.reconstruct(m.trellis, bits, K, N).astype(np.float64)
+    H = scipy.linalg.hadamard(128) / math.sqrt(128.0)
+    BH_K = np.kron(np.eye(K // 128), H)
+    BH_N = np.kron(np.eye(N // 128), H)
+    return np.diag(m.su.astype(np.float64)) @ BH_K @ W @ BH_N @ np.diag(m.sv.astype(np.float64)), W, BH_K, BH_N
+
+
+@pytest.mark.parametrize("K,N,bits", [(128, 128, 4), (256, 384, 3), (384, 256, 6)])
+def test_reconstruct_rotated_against_dense_fp64(oracle, K, N, bits):
+    m = synthetic.make_matrix(K, N, bits, seed=31 + bits)
+    wr = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv).astype(np.float64)
+    ref, _, _, _ = _dense_rotated_weight(oracle, m, K, N, bits)
+    # fp32 transforms then one fp16 rounding: within one fp16 spacing of the
+    # exact value everywhere, and its round-to-nearest almost everywhere
+    spacing = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    assert (np.abs(wr - ref) <= spacing).all()
+    assert np.mean(wr == ref.astype(np.float16).astype(np.float64)) > 0.99
+    # su and sv on the wrong sides (a plausible slip) is far outside that bound
+    W = oracle.reconstruct(m.trellis, bits, K, N).astype(np.float64)
+    H = scipy.linalg.hadamard(128) / math.sqrt(128.0)
+    wrong = np.kron(np.eye(K // 128), H) @ (W * m.sv.astype(np.float64)[None, :]) @ np.kron(np.eye(N // 128), H)
+    assert np.abs(wrong - ref).max() > 100 * spacing.max()
+
+
+def test_reconstruct_rotated_layouts_and_slices(oracle):
+    K, N, bits = 256, 512, 4
+    m = synthetic.make_matrix(K, N, bits, seed=37)
+    kn = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv, layout=0)
+    nk = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv, layout=1)
+    assert np.array_equal(kn.T.view(np.uint16), nk.view(np.uint16))
+    part = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv, n0=256, ncols=128)
+    assert np.array_equal(kn[:, 256:384].view(np.uint16), part.view(np.uint16))
+
+
+@pytest.mark.parametrize("K,N,M,bits", [(256, 384, 6, 4), (384, 256, 3, 3)])
+def test_weight_side_variant_is_the_same_layer(oracle, K, N, M, bits):
+    m = synthetic.make_matrix(K, N, bits, seed=41 + K)
+    x = synthetic.make_activations(M, K, seed=41)
+    ref_w, W, BH_K, BH_N = _dense_rotated_weight(oracle, m, K, N, bits)
+    x64 = x.astype(np.float64)
+    # exact arithmetic: moving both rotations onto the weight changes nothing
+    y_weight_side = x64 @ ref_w
+    y_layer_exact = ((x64 * m.su.astype(np.float64)[None, :]) @ BH_K @ W @ BH_N) * m.sv.astype(np.float64)[None, :]
+    rms = np.sqrt(np.mean(y_layer_exact ** 2))
+    assert np.abs(y_weight_side - y_layer_exact).max() / rms < 1e-12
+    # with the fp16-rounded rotated weight, against the layer oracle (which
+    # rounds x' instead): two independent fp16 roundings, each ~2.8e-4 rms of
+    # y per element, so the derived bound for this comparison is 3e-3
+    y_ws = oracle.matmul_f64(x, oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv))
+    y_layer = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert np.abs(y_ws - y_layer).max() / np.sqrt(np.mean(y_layer ** 2)) < 3e-3
+
+
 def test_linear_rejects_bad_shapes(oracle):
     m = synthetic.make_matrix(128, 128, 4, seed=0)
     x = synthetic.make_activations(1, 128, seed=0)
