@@ -387,7 +387,19 @@ def bench_prefill(args, torch, tql, peaks):
     tflops = flops / (t_call * 1e-3) / 1e12
     t_gemm = max(t_call - t_had - t_rec, 1e-6)
     peak = peaks["bf16_tflops"]  # fp16 and bf16 share the tensor-core rate
+    # weight-side rotation variant on the same call: rotated reconstruct + plain GEMM
+    wsr = torch.empty(tql.exl3_weight_rotated_workspace_bytes(K, N), dtype=torch.uint8, device="cuda")
+    t_wr = time_fn(torch, lambda: tql.exl3_linear_weight_rotated(x, M, K, mat.trellis, bits, N, N, mat.su, mat.sv,
+                                                                 y, tql.EXL3_F16, wsr), iters, 3)
+    t_rr = time_fn(torch, lambda: tql.exl3_reconstruct_rotated(mat.trellis, bits, K, N, 0, N, mat.su, mat.sv, wt,
+                                                               tql.EXL3_LAYOUT_NK), iters, 2)
+    weight_rotated = {"ms_per_call": round(t_wr, 4), "tflops": round(flops / (t_wr * 1e-3) / 1e12, 1),
+                      "frac": round(flops / (t_wr * 1e-3) / 1e12 / peak, 4),
+                      "reconstruct_rotated_ms": round(t_rr, 4),
+                      "reconstruct_rotated_gbs": round((mat.nbytes + N * K * 2) / (t_rr * 1e-3) / 1e9, 1)}
+    del wsr
     return {"geometry": "K=5120 N=17408 bits=4 M=2048", "ms_per_call": round(t_call, 4),
+            "weight_rotated": weight_rotated,
             "tflops": round(tflops, 1), "peak_tflops": peak, "frac": round(tflops / peak, 4),
             "peak_kind": f"of {peaks['source']} (cuBLAS bf16 burst; fp16 same rate)",
             "split_ms": {"hadamard": round(t_had, 4), "reconstruct": round(t_rec, 4), "gemm": round(t_gemm, 4)},

@@ -161,6 +161,40 @@ exl3_status exl3_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64
                              int64_t n0, int64_t n_cols, void *w, int layout, void *stream);
 
 /*
+ * Weight-side rotation variant ([P1] "Kernel measurements":
+ * reconstruct_had_slice). Moves both rotations and both scales onto the
+ * weight, W' = diag(su) . had_r_128(K) . W . had_r_128(N) . diag(sv), so the
+ * prefill-shaped layer is the plain product y = x . W'. The pages give no
+ * arithmetic for it; this library defines it per 128 x 128 block of W as
+ * fp32(w) -> fast WHT of each column along k (fp32, stages h = 1 .. 64)
+ * -> * fp32(su[k]) -> fast WHT of each row along n -> * 2^-7 (exact)
+ * -> * fp32(sv[n]) -> round to nearest even fp16, and the output is
+ * bit-exact with that definition.
+ *
+ * exl3_reconstruct_rotated: columns [n0, n0+n_cols) of W' into `w`
+ *   (fp16, `layout` as exl3_reconstruct); su: K fp16, sv: n_stored fp16.
+ *   K % 128 == 0, n0 % 128 == 0, n_cols % 128 == 0, n0 + n_cols <= n_stored.
+ *
+ * exl3_weight_rotated_workspace_bytes: scratch for
+ *   exl3_linear_weight_rotated (one 32768-column W'^T slice), 0 if invalid.
+ *
+ * exl3_linear_weight_rotated: y = x . W'[:, :n_gemm], reconstructing W' in
+ *   32768-column slices into the caller's workspace and running the
+ *   tensor-core GEMM without input or output rotation. x: M x K fp16 (not
+ *   rotated); y: M x n_gemm (`y_dtype`), ld = n_gemm; fp32 accumulation.
+ *   It differs from exl3_linear by where the fp16 roundings fall (W' instead
+ *   of x'): max|y - y_linear| / rms(y_linear) stays below 3e-3.
+ *   Errors as exl3_linear (EXL3_ERR_WORKSPACE_TOO_SMALL below the size above).
+ */
+exl3_status exl3_reconstruct_rotated(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored,
+                                     int64_t n0, int64_t n_cols, const void *su, const void *sv, void *w,
+                                     int layout, void *stream);
+size_t exl3_weight_rotated_workspace_bytes(int64_t K, int64_t n_gemm);
+exl3_status exl3_linear_weight_rotated(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits,
+                                       int64_t n_stored, int64_t n_gemm, const void *su, const void *sv, void *y,
+                                       int y_dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * exl3_linear: y = had_r_128( RNE_fp16(had_r_128(x * su)) . W[:, :n_gemm] )
  *                  * sv[:n_gemm]
  *   x:     M x K fp16.            su: K fp16.         sv: n_stored fp16.

@@ -119,6 +119,15 @@ def test_noalloc_limit_covers_mlp_geometries(lib):
     assert tql.exl3_linear_workspace_bytes_for(16, 5120, 248192, 6, 0, 152) > lim
 
 
+def test_weight_rotated_workspace_is_one_slice(lib):
+    # one 32768-column slice of W'^T (n rows rounded to 256, K fp16 each)
+    assert tql.exl3_weight_rotated_workspace_bytes(5120, 17408) == 17408 * 5120 * 2
+    assert tql.exl3_weight_rotated_workspace_bytes(5120, 248192) == 32768 * 5120 * 2
+    assert tql.exl3_weight_rotated_workspace_bytes(512, 384) == 512 * 512 * 2
+    assert tql.exl3_weight_rotated_workspace_bytes(100, 384) == 0
+    assert tql.exl3_weight_rotated_workspace_bytes(512, 100) == 0
+
+
 def test_invalid_arguments_are_rejected_before_any_launch(lib):
     good = 1 << 20  # a 16-byte aligned fake address; never dereferenced
     L = lib
@@ -147,6 +156,13 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert L.exl3_reconstruct(good, 4, 128, 256, 64, 128, good, 0, None) == 1
     assert L.exl3_reconstruct(good, 4, 128, 256, 0, 128, good, 2, None) == 1
     assert L.exl3_reconstruct(good, 4, 128, 256, 128, 256, good, 0, None) == 1
+    # weight-side rotation variant: K not a multiple of 128, slice out of range, workspace too small
+    assert L.exl3_reconstruct_rotated(good, 4, 64, 256, 0, 128, good, good, good, 0, None) == 1
+    assert L.exl3_reconstruct_rotated(good, 4, 128, 256, 128, 256, good, good, good, 0, None) == 1
+    assert L.exl3_reconstruct_rotated(good, 9, 128, 256, 0, 128, good, good, good, 0, None) == 3
+    assert L.exl3_reconstruct_rotated(good, 4, 128, 256, 0, 128, good + 8, good, good, 0, None) == 2
+    assert L.exl3_linear_weight_rotated(good, 4, 100, good, 4, 256, 256, good, good, good, 1, good, 1 << 30,
+                                        None) == 1
     # hadamard: cols not a multiple of 128
     assert L.exl3_hadamard128(good, good, None, 2, 100, None) == 1
     assert L.exl3_hadamard128(good, good + 8, None, 2, 128, None) == 2

@@ -377,6 +377,64 @@ def test_graph_capture_keeps_each_path(oracle):
     assert rel_err(y_big.cpu().numpy(), ref_b) <= TOL
 
 
+# ---------------------------------------------------------------------------
+# weight-side rotation variant
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [1, 3, 4, 6, 8])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("n0,n_cols", [(0, 384), (256, 128)])
+def test_reconstruct_rotated_bit_exact(oracle, bits, layout, n0, n_cols):
+    torch = torch_mod()
+    K, N = 256, 384
+    m = synthetic.make_matrix(K, N, bits, seed=50 + bits)
+    L = Layer(m)
+    shape = (K, n_cols) if layout == 0 else (n_cols, K)
+    w = torch.empty(shape, dtype=torch.float16, device="cuda")
+    tql.exl3_reconstruct_rotated(L.trellis, bits, K, N, n0, n_cols, L.su, L.sv, w, layout)
+    torch.cuda.synchronize()
+    ref = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv, n0, n_cols, layout)
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+
+
+@pytest.mark.parametrize("K,N,bits", [(256, 384, 4), (384, 256, 3), (640, 512, 6)])
+@pytest.mark.parametrize("M", [5, 130])
+def test_linear_weight_rotated(oracle, K, N, bits, M):
+    torch = torch_mod()
+    m = synthetic.make_matrix(K, N, bits, seed=60 + K + bits)
+    x = synthetic.make_activations(M, K, seed=M + 61)
+    L = Layer(m)
+    ws = torch.empty(tql.exl3_weight_rotated_workspace_bytes(K, N), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tql.exl3_linear_weight_rotated(to_dev(x), M, K, L.trellis, bits, N, N, L.su, L.sv, y, tql.EXL3_F32, ws)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy()
+    wr = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(got, oracle.matmul_f64(x, wr)) <= TOL
+    # the same layer as exl3_linear, within the budget derived for moving the
+    # fp16 rounding from x' to W'
+    assert rel_err(got, oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)) <= 3e-3
+
+
+def test_weight_rotated_full_gate_geometry_sampled(oracle):
+    torch = torch_mod()
+    K, N, bits, M = 5120, 17408, 4, 256
+    m = synthetic.make_matrix(K, N, bits, seed=2)
+    x = synthetic.make_activations(M, K, seed=2)
+    L = Layer(m)
+    ws = torch.empty(tql.exl3_weight_rotated_workspace_bytes(K, N), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tql.exl3_linear_weight_rotated(to_dev(x), M, K, L.trellis, bits, N, N, L.su, L.sv, y, tql.EXL3_F32, ws)
+    w = torch.empty((128, K), dtype=torch.float16, device="cuda")
+    for b in (0, 77, N // 128 - 1):
+        tql.exl3_reconstruct_rotated(L.trellis, bits, K, N, 128 * b, 128, L.su, L.sv, w, tql.EXL3_LAYOUT_NK)
+        torch.cuda.synchronize()
+        ref_w = oracle.reconstruct_rotated(m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128, 1)
+        assert np.array_equal(w.cpu().numpy().view(np.uint16), ref_w.view(np.uint16)), b
+        ref = oracle.matmul_f64(x, ref_w.T)
+        assert rel_err(y[:, 128 * b:128 * b + 128].cpu().numpy(), ref) <= TOL, b
+
+
 @pytest.mark.parametrize("M", [1, 16, 40])
 def test_decode_stack_graph_matches_eager(oracle, M):
     """A whole decode step of a small MLP stack (3 layers of gate, up,

@@ -18,7 +18,8 @@ __all__ = [
     "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_linear_workspace_bytes_for",
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
-    "exl3_linear_decode_noalloc", "exl3_silu_mul", "HEADER_SYMBOLS",
+    "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
+    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated", "HEADER_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,8 @@ HEADER_SYMBOLS = (
     "exl3_decode_plan", "exl3_linear_workspace_bytes_for", "exl3_linear_workspace_bytes",
     "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct", "exl3_linear",
     "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
-    "exl3_linear_decode_noalloc", "exl3_silu_mul",
+    "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
+    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated",
 )
 
 
@@ -95,6 +97,11 @@ def load():
             "exl3_silu_mul": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
             "exl3_linear_decode_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i64, _vp, _vp,
                                                           _vp, ctypes.c_int, _vp]),
+            "exl3_reconstruct_rotated": (ctypes.c_int, [_vp, ctypes.c_int, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                        ctypes.c_int, _vp]),
+            "exl3_weight_rotated_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
+            "exl3_linear_weight_rotated": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i64, _vp, _vp,
+                                                          _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -183,6 +190,26 @@ def exl3_reconstruct(trellis, bits: int, K: int, n_stored: int, n0: int, n_cols:
                      layout: int = EXL3_LAYOUT_KN, stream=None) -> None:
     _check(load().exl3_reconstruct(_ptr(trellis), int(bits), int(K), int(n_stored), int(n0), int(n_cols),
                                    _ptr(w), int(layout), _stream(stream)), "exl3_reconstruct")
+
+
+def exl3_reconstruct_rotated(trellis, bits: int, K: int, n_stored: int, n0: int, n_cols: int, su, sv, w,
+                             layout: int = EXL3_LAYOUT_KN, stream=None) -> None:
+    _check(load().exl3_reconstruct_rotated(_ptr(trellis), int(bits), int(K), int(n_stored), int(n0), int(n_cols),
+                                           _ptr(su), _ptr(sv), _ptr(w), int(layout), _stream(stream)),
+           "exl3_reconstruct_rotated")
+
+
+def exl3_weight_rotated_workspace_bytes(K: int, n_gemm: int) -> int:
+    return int(load().exl3_weight_rotated_workspace_bytes(int(K), int(n_gemm)))
+
+
+def exl3_linear_weight_rotated(x, M: int, K: int, trellis, bits: int, n_stored: int, n_gemm: int, su, sv, y,
+                               y_dtype: int, workspace, workspace_bytes: int | None = None, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check(load().exl3_linear_weight_rotated(_ptr(x), int(M), int(K), _ptr(trellis), int(bits), int(n_stored),
+                                             int(n_gemm), _ptr(su), _ptr(sv), _ptr(y), int(y_dtype),
+                                             _ptr(workspace), int(nbytes), _stream(stream)),
+           "exl3_linear_weight_rotated")
 
 
 def exl3_linear(x, M: int, K: int, trellis, bits: int, n_stored: int, n_gemm: int, su, sv, y, y_dtype: int,

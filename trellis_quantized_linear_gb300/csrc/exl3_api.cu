@@ -209,6 +209,7 @@ exl3_status exl3_init(int device) {
   info.status = static_cast<int *>(status);
   if (cudaMemset(info.status, 0, sizeof(int)) != cudaSuccess) return EXL3_ERR_CUDA;
   if (init_rotate_kernels() != cudaSuccess || init_reconstruct_kernels() != cudaSuccess ||
+      init_reconstruct_rotated_kernels() != cudaSuccess ||
       init_decode_kernels() != cudaSuccess || init_prefill_kernels() != cudaSuccess ||
       init_fused_kernels() != cudaSuccess)
     return EXL3_ERR_CUDA;
@@ -295,6 +296,72 @@ exl3_status exl3_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64
   if (!dev) return EXL3_ERR_NOT_INITIALIZED;
   return from_cuda(launch_reconstruct(trellis, bits, K, n_stored, n0, n_cols, w, layout, dev->num_sms,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+exl3_status exl3_reconstruct_rotated(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored, int64_t n0,
+                                     int64_t n_cols, const void *su, const void *sv, void *w, int layout,
+                                     void *stream) {
+  if (K <= 0 || K % 128 || K > 131072 || n_stored <= 0 || n_stored % 128 || n_stored > ((int64_t)1 << 24) ||
+      n0 < 0 || n0 % 128 || n_cols < 0 || n_cols % 128 || n0 + n_cols > n_stored ||
+      (layout != EXL3_LAYOUT_KN && layout != EXL3_LAYOUT_NK))
+    return EXL3_ERR_INVALID_ARG;
+  if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
+  if (!aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(w)) return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  return from_cuda(launch_reconstruct_rotated(trellis, bits, K, n_stored, n0, n_cols, su, sv, w, layout,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+size_t exl3_weight_rotated_workspace_bytes(int64_t K, int64_t n_gemm) {
+  if (K <= 0 || K % 128 || K > 131072 || n_gemm <= 0 || n_gemm % 128 || n_gemm > ((int64_t)1 << 24)) return 0;
+  const int64_t cols = n_gemm < EXL3_RECONSTRUCT_CHUNK_COLS ? n_gemm : EXL3_RECONSTRUCT_CHUNK_COLS;
+  return (size_t)((cols + 255) / 256 * 256) * (size_t)K * 2;
+}
+
+exl3_status exl3_linear_weight_rotated(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits,
+                                       int64_t n_stored, int64_t n_gemm, const void *su, const void *sv, void *y,
+                                       int y_dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  if (y_dtype != EXL3_F16 && y_dtype != EXL3_F32) return EXL3_ERR_INVALID_ARG;
+  if (M < 0 || M > (int64_t)1 << 31 || !shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
+  if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
+  if (!aligned16(x) || !aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(y) ||
+      !aligned16(workspace))
+    return EXL3_ERR_ALIGNMENT;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+  const size_t need = exl3_weight_rotated_workspace_bytes(K, n_gemm);
+  if (need == 0) return EXL3_ERR_INVALID_ARG;
+  if (need > workspace_bytes) return EXL3_ERR_WORKSPACE_TOO_SMALL;
+  if (M == 0) return EXL3_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t ysz = y_dtype == EXL3_F32 ? 4 : 2;
+  const int64_t chunk_rows = (int64_t)(need / ((size_t)K * 2));
+  for (int64_t c0 = 0; c0 < n_gemm; c0 += EXL3_RECONSTRUCT_CHUNK_COLS) {
+    const int64_t nc = (n_gemm - c0) < EXL3_RECONSTRUCT_CHUNK_COLS ? (n_gemm - c0) : EXL3_RECONSTRUCT_CHUNK_COLS;
+    cudaError_t e = launch_reconstruct_rotated(trellis, bits, K, n_stored, c0, nc, su, sv, workspace,
+                                               EXL3_LAYOUT_NK, st);
+    if (e != cudaSuccess) return EXL3_ERR_CUDA;
+    PrefillLaunch p;
+    p.xr = x;
+    p.xr_rows = M;
+    p.M = M;
+    p.K = K;
+    p.wt = workspace;
+    p.chunk_rows = chunk_rows;
+    p.nc = nc;
+    p.sv = sv;  // unused: the weight carries sv
+    p.y = static_cast<uint8_t *>(y) + (size_t)c0 * ysz;
+    p.ldy = n_gemm;
+    p.y_f32 = y_dtype == EXL3_F32;
+    p.n_valid_local = nc;
+    p.status = dev->status;
+    p.num_sms = dev->num_sms;
+    p.rotate = 0;
+    e = launch_prefill_gemm(p, st);
+    if (e != cudaSuccess) return EXL3_ERR_CUDA;
+  }
+  return EXL3_OK;
 }
 
 exl3_status exl3_linear(const void *x, int64_t M, int64_t K, const uint16_t *trellis, int bits, int64_t n_stored,

@@ -76,6 +76,7 @@ struct PrefillLaunch {
   int64_t n_valid_local;  // columns >= this are written as -inf
   int *status;
   int num_sms;
+  int rotate = 1;         // 0: plain store of x . W (weight-side rotation variant), no sv
 };
 
 struct FusedLaunch {
@@ -102,6 +103,10 @@ cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t 
                                    int y_f32, int64_t n_gemm, int64_t n_valid, int rows, int64_t P, int64_t TS,
                                    int units_per_block, int all_blocks, cudaStream_t st);
 cudaError_t init_reconstruct_kernels();
+cudaError_t init_reconstruct_rotated_kernels();
+cudaError_t launch_reconstruct_rotated(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored, int64_t n0,
+                                       int64_t n_cols, const void *su, const void *sv, void *w, int layout,
+                                       cudaStream_t st);
 cudaError_t init_decode_kernels();
 cudaError_t init_prefill_kernels();
 

@@ -51,30 +51,34 @@ struct PrefillParams {
   int *status;
   int64_t ldy, n_valid_local;
   int M, nc, K, y_f32, tiles_m, tiles_n;
+  int rotate;  // 0: the weight already carries both rotations and sv
 };
 
-// In-register orthonormal had_r_128 of one row block, then * sv, mask, store.
+// In-register orthonormal had_r_128 of one row block, then * sv, mask, store
+// (rotation and sv skipped for a pre-rotated weight).
 __device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillParams &p, int64_t row, int col0) {
+  if (p.rotate) {
 #pragma unroll
-  for (int h = 1; h < 128; h <<= 1) {
+    for (int h = 1; h < 128; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      if (!(i & h)) {
-        float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
+      for (int i = 0; i < 128; ++i) {
+        if (!(i & h)) {
+          float a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
       }
     }
-  }
-  const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
+    const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
 #pragma unroll
-  for (int a = 0; a < 16; ++a) {
-    uint4 raw = __ldg(svp + a);
-    const __half *h = reinterpret_cast<const __half *>(&raw);
+    for (int a = 0; a < 16; ++a) {
+      uint4 raw = __ldg(svp + a);
+      const __half *h = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = 8 * a + e;
-      v[c] = (col0 + c < p.n_valid_local) ? v[c] * (__half2float(h[e]) * kInvSqrt128) : -INFINITY;
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * a + e;
+        v[c] = (col0 + c < p.n_valid_local) ? v[c] * (__half2float(h[e]) * kInvSqrt128) : -INFINITY;
+      }
     }
   }
   if (row >= p.M) return;
@@ -307,6 +311,7 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   p.status = L.status;
   p.ldy = L.ldy;
   p.n_valid_local = L.n_valid_local;
+  p.rotate = L.rotate;
   p.M = (int)L.M;
   p.nc = (int)L.nc;
   p.K = (int)L.K;
