@@ -93,13 +93,14 @@ def _owner(z, P, TS):
 @pytest.mark.parametrize("K,N", [(5120, 17408), (17408, 5120), (5120, 248192), (512, 512), (128, 128)])
 @pytest.mark.parametrize("sms", [148, 152, 160])
 def test_decode_plan_invariants(lib, K, N, sms):
-    """Stream-K split: 16 warps per CTA, one CTA per SM, every warp at least
+    """Stream-K split: 12 warps per CTA, one CTA per SM, every warp at least
     one slab; slots = the most warps sharing one 128-column n-block."""
+    W = 12
     slots, ctas = tql.exl3_decode_plan(K, N, sms)
     KT, NB = K // 16, N // 128
     TS = NB * KT
-    P = min(16 * sms, TS)
-    assert ctas == -(-P // 16) and ctas <= sms
+    P = min(W * sms, TS)
+    assert ctas == -(-P // W) and ctas <= sms
     want = max(_owner((nb + 1) * KT - 1, P, TS) - _owner(nb * KT, P, TS) + 1 for nb in range(NB))
     assert slots == want
     # each warp owns a non-empty, contiguous range and the ranges tile the slab space
@@ -109,7 +110,7 @@ def test_decode_plan_invariants(lib, K, N, sms):
 
 def test_decode_plan_gate_geometry_fills_every_sm(lib):
     slots, ctas = tql.exl3_decode_plan(5120, 17408, 152)
-    assert ctas == 152 and slots == 19
+    assert ctas == 152 and slots == 15
 
 
 def test_noalloc_limit_covers_mlp_geometries(lib):

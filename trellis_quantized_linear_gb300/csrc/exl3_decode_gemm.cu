@@ -42,12 +42,12 @@
 
 // Tuning knobs (compile-time): warps per CTA for <= 8 rows.
 #ifndef EXL3_DECODE_WARPS_M8
-#define EXL3_DECODE_WARPS_M8 16
+#define EXL3_DECODE_WARPS_M8 12
 #endif
 // Packing of two decoded fp16 weights into one mma register, per variant
 // (0: byte permute on the integer pipe; 1: multiply-add on the fp16 pipe).
 #ifndef EXL3_DECODE_PACK_FMA_M8
-#define EXL3_DECODE_PACK_FMA_M8 0
+#define EXL3_DECODE_PACK_FMA_M8 1
 #endif
 #ifndef EXL3_DECODE_PACK_FMA_M16
 #define EXL3_DECODE_PACK_FMA_M16 1
