@@ -270,13 +270,13 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
  * plugin inside a host program that owns every device buffer, or code that
  * must not call cudaMalloc at run time because it synchronises the whole
  * device. The caller passes only inputs and outputs; the split-K partial
- * sums and rotated activations live in a fixed 16 MiB buffer inside the
+ * sums and rotated activations live in a fixed 24 MiB buffer inside the
  * library (a static device array that every GPU which loads libexl3.so
  * keeps until the process exits). The pages have no counterpart to this
  * entry point.
  *   Arguments as exl3_linear, without m_threshold and workspace.
  *   Limit: exl3_linear_workspace_bytes(16, K, n_gemm, bits, 0) must not
- *   exceed 16 MiB (the MLP projections fit; a 248192-wide logits layer does
+ *   exceed 24 MiB (the MLP projections fit; a 248192-wide logits layer does
  *   not); larger problems return EXL3_ERR_NOALLOC_TOO_LARGE and launch
  *   nothing.
  *   The first call on a device looks up the buffer's device address, so

@@ -229,7 +229,7 @@ const char *exl3_status_string(int status) {
     case EXL3_ERR_NOT_INITIALIZED: return "exl3_init was not called for the current device";
     case EXL3_ERR_CUDA: return "CUDA runtime error or failed launch";
     case EXL3_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
-    case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed 16 MiB no-alloc buffer";
+    case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed 24 MiB no-alloc buffer";
     default: return "unknown status";
   }
 }

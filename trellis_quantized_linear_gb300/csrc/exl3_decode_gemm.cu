@@ -44,6 +44,10 @@
 #ifndef EXL3_DECODE_WARPS_M8
 #define EXL3_DECODE_WARPS_M8 12
 #endif
+// ... and for 9..16 rows.
+#ifndef EXL3_DECODE_WARPS_M16
+#define EXL3_DECODE_WARPS_M16 12
+#endif
 // Packing of two decoded fp16 weights into one mma register, per variant
 // (0: byte permute on the integer pipe; 1: multiply-add on the fp16 pipe).
 #ifndef EXL3_DECODE_PACK_FMA_M8
@@ -77,7 +81,7 @@ namespace {
 
 template <int BITS, int MT>
 struct DecodeCfg {
-  static constexpr int kWarps = MT == 1 ? EXL3_DECODE_WARPS_M8 : 8;  // warps per CTA
+  static constexpr int kWarps = MT == 1 ? EXL3_DECODE_WARPS_M8 : EXL3_DECODE_WARPS_M16;  // warps per CTA
   static constexpr int kSeg = 256 * BITS;                    // trellis bytes per slab
   static constexpr int kChunk = BITS <= 4 ? EXL3_DECODE_CHUNK : (EXL3_DECODE_CHUNK + 1) / 2;  // slabs per copy
   static constexpr int kStages = MT == 1 ? EXL3_DECODE_STAGES_M8 : 3;  // ring stages (chunks) per warp

@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoallocScratchBytes = size_t(24) << 20;  // 24 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
