@@ -57,19 +57,26 @@ constexpr int F_B_STAGE = F_BN * F_BK * 2;   // one 128 x 64 fp16 W^T tile (128-
 constexpr int F_A_TILE = 128 * F_BK * 2;     // 128 rows x 64 fp16 of x' (128-byte swizzle)
 
 // MTILES = ceil(npad / 128) sizes the x' region; npad is a runtime value and
-// the region holds 32 KB / (npad * 128 B) * MTILES stages (2 .. 8).
+// the region holds kARegion / (npad * 128 B) stages (2 .. 8).
 template <int BITS, int MTILES>
 struct FusedCfg {
   static constexpr int kSeg = 256 * BITS;
-  // Trellis bytes each decoder warp keeps in flight.
-  static constexpr int kRingBytes = 3072;
+  // Trellis bytes each decoder warp keeps in flight (at least two slabs):
+  // 16 warps x 2 KB per SM covers the HBM latency at the rate the decoders
+  // consume.
+  static constexpr int kRingBytes = 2048;
   static constexpr int kRD = kRingBytes / kSeg < 2 ? 2 : kRingBytes / kSeg;
-  static constexpr int kARegion = 2 * MTILES * F_A_TILE;
+  static constexpr int kBudget = 227 * 1024 - 2048 - 2048;
+  static constexpr int kRest = kBudget - F_DEC_WARPS * kRD * kSeg;
+  // x' region: three stages at the widest npad of this variant when at least
+  // five W^T stages still fit (the MMA issuer batches ready k steps only
+  // with three or more x' stages), else two.
+  static constexpr int kA3 = 3 * MTILES * F_A_TILE, kA2 = 2 * MTILES * F_A_TILE;
+  static constexpr int kARegion = (kRest - kA3) / F_B_STAGE >= F_GROUPS + 1 ? kA3 : kA2;
   // W^T stages: the decoder groups run in rounds of F_GROUPS k steps; with
   // 2 * F_GROUPS stages a group only needs the stage the MMA was handed a
   // whole round earlier. Take as many as shared memory holds, up to that.
-  static constexpr int kBudget = 227 * 1024 - 2048 - 2048;
-  static constexpr int kSBFit = (kBudget - kARegion - F_DEC_WARPS * kRD * kSeg) / F_B_STAGE;
+  static constexpr int kSBFit = (kRest - kARegion) / F_B_STAGE;
   static constexpr int kSB = kSBFit > 2 * F_GROUPS ? 2 * F_GROUPS : kSBFit;
   static constexpr int kOffB = kARegion;
   static constexpr int kOffD = kOffB + kSB * F_B_STAGE;
@@ -505,6 +512,22 @@ cudaError_t launch_mt(int bits, const CUtensorMap &tmA, const FusedParams &fp, i
 
 int64_t owner_h(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
 
+template <int MTILES>
+int a_region_mt(int bits) {
+  switch (bits) {
+    case 1: return FusedCfg<1, MTILES>::kARegion;
+    case 2: return FusedCfg<2, MTILES>::kARegion;
+    case 3: return FusedCfg<3, MTILES>::kARegion;
+    case 4: return FusedCfg<4, MTILES>::kARegion;
+    case 5: return FusedCfg<5, MTILES>::kARegion;
+    case 6: return FusedCfg<6, MTILES>::kARegion;
+    case 7: return FusedCfg<7, MTILES>::kARegion;
+    default: return FusedCfg<8, MTILES>::kARegion;
+  }
+}
+
+int a_region_bytes(int bits, int mtiles) { return mtiles == 1 ? a_region_mt<1>(bits) : a_region_mt<2>(bits); }
+
 }  // namespace
 
 FusedPlan fused_plan(int64_t n_blocks, int64_t K, int num_sms) {
@@ -563,7 +586,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch &L, cudaStream_t st) {
   fp.smax = (int)L.plan.smax;
   fp.npad = npad;
   fp.tmem_cols = tmem_cols;
-  fp.nsa = (2 * MTILES * F_A_TILE) / (npad * F_BK * 2);
+  fp.nsa = a_region_bytes(L.bits, MTILES) / (npad * F_BK * 2);
   if (fp.nsa > F_MAX_SA) fp.nsa = F_MAX_SA;
   cudaError_t e = MTILES == 1 ? launch_mt<1>(L.bits, tmA, fp, fp.P, st) : launch_mt<2>(L.bits, tmA, fp, fp.P, st);
   if (e != cudaSuccess) return e;
