@@ -22,7 +22,8 @@ Also measured in the same run (reported as sub-objects of the JSON line):
 cores on a bounded sample of the same workload, as the reference arm.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-       [--quick] [--no-extras]
+       [--quick] [--no-extras] [--extras a,b,...]
+       python bench.py --profile-call K,N,BITS,M[,REPS]   (profiling aid, no JSON)
 """
 from __future__ import annotations
 
@@ -63,6 +64,9 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--quick", action="store_true", help="smaller extras (for profiling runs)")
     p.add_argument("--no-extras", action="store_true", help="headline workload only")
+    p.add_argument("--profile-call", default=None, metavar="K,N,BITS,M[,REPS]",
+                   help="profiling aid: run the decode-shaped exl3_linear REPS (default 4) times on one seeded "
+                        "matrix of that shape and exit (no JSON line)")
     p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack,decode_stack",
                    help="comma-separated sub-measurements to run after the headline")
     return p.parse_args()
@@ -409,7 +413,7 @@ def bench_prefill(args, torch, tql, peaks):
 
 def bench_crossover(args, torch, tql):
     out = {}
-    Ms = (16, 32, 64, 128) if args.quick else (16, 32, 48) + tuple(synthetic.PREFILL_MS)
+    Ms = (16, 32, 64, 128) if args.quick else tuple(sorted(set((16, 32, 48, 384, 512, 768) + synthetic.PREFILL_MS)))
     for gm in synthetic.PREFILL_GEOMS:
         K, N, bits = gm["K"], gm["N"], 4
         mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
@@ -501,7 +505,12 @@ def bench_mlp_stack(args, torch, tql):
 
         first_bad = one_pass(check=True)
         torch.cuda.synchronize()
-        ms = time_fn(torch, one_pass, 2, 1)
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        clocks.mark_start()
+        ms = time_fn(torch, one_pass, 4, 1)
+        clocks.mark_end()
+        clk = clocks.stop()
         # split from component timings of each geometry
         split = {"hadamard": 0.0, "reconstruct": 0.0, "gemm": 0.0}
         for (K, N), times in (((d, f), 2), ((f, d), 1)):
@@ -522,7 +531,7 @@ def bench_mlp_stack(args, torch, tql):
         out[f"bits{bits}"] = {"layers": L, "ms_per_pass": round(ms, 3), "tok_per_s": round(M / (ms * 1e-3), 1),
                               "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                               "split_ms": {k: round(v, 3) for k, v in split.items()},
-                              "first_nonfinite_layer": first_bad,
+                              "first_nonfinite_layer": first_bad, "clocks": clk,
                               "trellis_gb": round(sum(m["tr"].numel() * 2 for lay in layers for m in lay) / 1e9, 2)}
         del layers, ws
         torch.cuda.empty_cache()
@@ -592,9 +601,11 @@ def bench_decode_stack(args, torch, tql, peaks):
 # CPU oracle: baseline leg and reference arm
 # ---------------------------------------------------------------------------
 
-def oracle_sample(budget_s: float):
+def oracle_sample(budget_s: float, total_s: float = 0.0):
     """Times the oracle on a column sample of the decode workload (M=16
-    rows, full K), doubling the sample until one call takes >= budget_s."""
+    rows, full K), doubling the sample until one call takes >= budget_s (or
+    covers all columns), then repeating that call until total_s seconds of
+    CPU work have run."""
     import oracle
     oracle.build()
     g = synthetic.GATE_DECODE
@@ -609,10 +620,36 @@ def oracle_sample(budget_s: float):
         if dt >= budget_s or cols >= N:
             break
         cols = min(N, cols * 2)
+    calls, total = 1, dt
+    while total < total_s:
+        t0 = time.perf_counter()
+        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+        total += time.perf_counter() - t0
+        calls += 1
     bytes_ = K * cols * bits // 8
-    return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"one M=16 call over columns [0, {cols}) of K=5120 N=17408 bits=4 "
-                      f"({bytes_} trellis bytes), {dt:.2f} s", "cols": cols, "seconds": dt}
+    return {"value": bytes_ * calls / total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{calls} M=16 calls over columns [0, {cols}) of K=5120 N=17408 bits=4 "
+                      f"({bytes_} trellis bytes each), {total:.1f} s", "cols": cols, "seconds": dt}
+
+
+def profile_call(spec: str):
+    """Runs exl3_linear (decode-shaped, m_threshold 0) a few times at one
+    shape, for capturing its kernels under a profiler."""
+    import torch
+    import trellis_quantized_linear_gb300 as tql
+    vals = [int(v) for v in spec.split(",")]
+    K, N, bits, M = vals[:4]
+    reps = vals[4] if len(vals) > 4 else 4
+    torch.cuda.set_device(0)
+    tql.build()
+    tql.exl3_init(0)
+    mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
+    x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = make_ws(torch, tql, M, K, N, bits, 0)
+    for _ in range(reps):
+        call_linear(tql, x, M, mat, y, 0, ws, tql.EXL3_F16)
+    torch.cuda.synchronize()
 
 
 def run_reference(args, dist):
@@ -656,6 +693,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, dist)
         return
+    if args.profile_call:
+        profile_call(args.profile_call)
+        return
     import torch
     import trellis_quantized_linear_gb300 as tql
     if world > 1:
@@ -685,7 +725,7 @@ def main():
     status = tql.exl3_get_device_status()
     cpu = None
     if rank == 0 and world == 1:
-        cpu = oracle_sample(1.0)
+        cpu = oracle_sample(1.0, 10.0)
         cpu = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cpu.items() if k not in ("cols", "seconds")}
     if rank == 0:
         line = {
