@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     const int64_t left = z1 - z;
     const int len = (int)((KT - tk) < CHK ? ((int64_t)(KT - tk) < left ? (KT - tk) : left)
                                           : (CHK < left ? CHK : left));
-#pragma unroll 1
+#pragma unroll(MT == 1 ? 2 : 1)  // two slabs per iteration for <= 8 rows (measured: 1-1.5 % faster)
     for (int i = 0; i < len; ++i) {
     uint32_t own[2 * BITS];
     load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
