@@ -217,8 +217,9 @@ def test_workspace_too_small_is_rejected():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("thr", [DECODE, PREFILL])
-def test_logits_mask_and_argmax_small(oracle, thr):
-    K, n_stored, n_gemm, bits, M = 256, 640, 512, 6, 6
+@pytest.mark.parametrize("M", [6, 40])  # decode-shaped: the 16-row kernel / the tensor-core kernel
+def test_logits_mask_and_argmax_small(oracle, thr, M):
+    K, n_stored, n_gemm, bits = 256, 640, 512, 6
     m = synthetic.make_matrix(K, n_stored, bits, seed=4)
     x = synthetic.make_activations(M, K, seed=4)
     raw = oracle.linear(x, m.trellis, bits, K, n_stored, m.su, m.sv, 0, n_gemm)
@@ -269,7 +270,7 @@ def test_prefill_full_size_sampled(oracle, geom):
         assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, b
 
 
-@pytest.mark.parametrize("M", [1, 16, 2048])
+@pytest.mark.parametrize("M", [1, 16, 64, 2048])
 def test_logits_full_size(oracle, M):
     c = synthetic.LOGITS
     K, n_stored, n_gemm, n_dec, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
