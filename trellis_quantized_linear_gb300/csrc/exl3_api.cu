@@ -102,7 +102,10 @@ exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const vo
   if (e != cudaSuccess) return EXL3_ERR_CUDA;
   for (int64_t c0 = 0; c0 < n_gemm; c0 += EXL3_RECONSTRUCT_CHUNK_COLS) {
     const int64_t nc = (n_gemm - c0) < EXL3_RECONSTRUCT_CHUNK_COLS ? (n_gemm - c0) : EXL3_RECONSTRUCT_CHUNK_COLS;
-    e = launch_reconstruct(trellis, bits, K, n_stored, c0, nc, wchunk, EXL3_LAYOUT_NK, dev->num_sms, st);
+    // The first chunk may run alongside the input rotation (independent
+    // operands); later chunks follow the GEMM that reads the chunk buffer.
+    e = launch_reconstruct(trellis, bits, K, n_stored, c0, nc, wchunk, EXL3_LAYOUT_NK, dev->num_sms, st,
+                           c0 == 0 ? 1 : 0);
     if (e != cudaSuccess) return EXL3_ERR_CUDA;
     PrefillLaunch p;
     p.xr = xr;

@@ -112,9 +112,11 @@ cudaError_t init_prefill_kernels();
 
 cudaError_t launch_hadamard128(const void *x, void *y, const void *pre, int64_t rows, int64_t cols,
                                int num_sms, cudaStream_t st);
+// overlap: launched right after the input rotation of the prefill path, which
+// it may run alongside (waits for it before exiting).
 cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored,
                                int64_t n0, int64_t n_cols, void *w, int layout, int num_sms,
-                               cudaStream_t st);
+                               cudaStream_t st, int overlap = 0);
 cudaError_t launch_decode_gemm(const DecodeLaunch &p, cudaStream_t st);
 cudaError_t launch_prefill_gemm(const PrefillLaunch &p, cudaStream_t st);
 cudaError_t launch_argmax(const float *logits, int64_t M, int64_t n, int32_t *argmax,

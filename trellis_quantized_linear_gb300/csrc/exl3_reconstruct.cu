@@ -16,11 +16,15 @@
 namespace exl3 {
 
 // LAYOUT 0 (KN): w[k][j], ld = n_cols.  LAYOUT 1 (NK): w[j][k], ld = K.
+// With `overlap` set the kernel was launched as a programmatic dependent of
+// the input rotation (which neither reads nor writes its operands): it runs
+// alongside it and only waits for it before exiting, so that the GEMM queued
+// after this kernel sees both finished.
 template <int BITS, int LAYOUT>
 __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restrict__ trellis,
                                                           int64_t tiles_n, int64_t tk_count,
                                                           int64_t nb0, int64_t nbc, __half *w,
-                                                          int64_t K, int64_t n_cols) {
+                                                          int64_t K, int64_t n_cols, int overlap) {
   constexpr int kTileBytes = 32 * BITS;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
@@ -63,6 +67,7 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restr
       });
     }
   }
+  if (overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int BITS>
@@ -85,19 +90,33 @@ cudaError_t init_reconstruct_kernels() {
   return init_bits<8>();
 }
 
+template <int BITS, int LAYOUT>
+static cudaError_t launch_one(const uint8_t *t, int64_t tiles_n, int64_t tkc, int64_t nb0, int64_t nbc,
+                              __half *w, int64_t K, int64_t n_cols, unsigned grid, int overlap, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, reconstruct_kernel<BITS, LAYOUT>, t, tiles_n, tkc, nb0, nbc, w, K, n_cols,
+                            overlap);
+}
+
 template <int BITS>
-static void launch_bits(const uint8_t *t, int64_t tiles_n, int64_t tkc, int64_t nb0, int64_t nbc,
-                        __half *w, int64_t K, int64_t n_cols, int layout, unsigned grid,
-                        cudaStream_t st) {
-  if (layout == 0)
-    reconstruct_kernel<BITS, 0><<<grid, 256, 0, st>>>(t, tiles_n, tkc, nb0, nbc, w, K, n_cols);
-  else
-    reconstruct_kernel<BITS, 1><<<grid, 256, 0, st>>>(t, tiles_n, tkc, nb0, nbc, w, K, n_cols);
+static cudaError_t launch_bits(const uint8_t *t, int64_t tiles_n, int64_t tkc, int64_t nb0, int64_t nbc,
+                               __half *w, int64_t K, int64_t n_cols, int layout, unsigned grid, int overlap,
+                               cudaStream_t st) {
+  return layout == 0 ? launch_one<BITS, 0>(t, tiles_n, tkc, nb0, nbc, w, K, n_cols, grid, overlap, st)
+                     : launch_one<BITS, 1>(t, tiles_n, tkc, nb0, nbc, w, K, n_cols, grid, overlap, st);
 }
 
 cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored,
                                int64_t n0, int64_t n_cols, void *w, int layout, int num_sms,
-                               cudaStream_t st) {
+                               cudaStream_t st, int overlap) {
   const int64_t tkc = K / 16, nbc = n_cols / 128;
   const int64_t slabs = tkc * nbc;
   if (slabs == 0) return cudaSuccess;
@@ -108,17 +127,16 @@ cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int
   __half *wp = static_cast<__half *>(w);
   const int64_t tiles_n = n_stored / 16, nb0 = n0 / 128;
   switch (bits) {
-    case 1: launch_bits<1>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 7: launch_bits<7>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 2: launch_bits<2>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 3: launch_bits<3>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 4: launch_bits<4>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 5: launch_bits<5>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 6: launch_bits<6>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
-    case 8: launch_bits<8>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, st); break;
+    case 1: return launch_bits<1>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 2: return launch_bits<2>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 3: return launch_bits<3>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 4: return launch_bits<4>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 5: return launch_bits<5>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 6: return launch_bits<6>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 7: return launch_bits<7>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
+    case 8: return launch_bits<8>(t, tiles_n, tkc, nb0, nbc, wp, K, n_cols, layout, (unsigned)grid, overlap, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace exl3
