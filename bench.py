@@ -64,9 +64,9 @@ def parse_args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--quick", action="store_true", help="smaller extras (for profiling runs)")
     p.add_argument("--no-extras", action="store_true", help="headline workload only")
-    p.add_argument("--profile-call", default=None, metavar="K,N,BITS,M[,REPS]",
-                   help="profiling aid: run the decode-shaped exl3_linear REPS (default 4) times on one seeded "
-                        "matrix of that shape and exit (no JSON line)")
+    p.add_argument("--profile-call", default=None, metavar="K,N,BITS,M[,REPS[,THRESHOLD]]",
+                   help="profiling aid: run exl3_linear REPS (default 4) times on one seeded matrix of that shape "
+                        "with that m_threshold (default 0: decode-shaped) and exit (no JSON line)")
     p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack,decode_stack",
                    help="comma-separated sub-measurements to run after the headline")
     return p.parse_args()
@@ -633,22 +633,23 @@ def oracle_sample(budget_s: float, total_s: float = 0.0):
 
 
 def profile_call(spec: str):
-    """Runs exl3_linear (decode-shaped, m_threshold 0) a few times at one
-    shape, for capturing its kernels under a profiler."""
+    """Runs exl3_linear a few times at one shape (decode-shaped unless a
+    threshold <= M is given), for capturing its kernels under a profiler."""
     import torch
     import trellis_quantized_linear_gb300 as tql
     vals = [int(v) for v in spec.split(",")]
     K, N, bits, M = vals[:4]
     reps = vals[4] if len(vals) > 4 else 4
+    thr = vals[5] if len(vals) > 5 else 0
     torch.cuda.set_device(0)
     tql.build()
     tql.exl3_init(0)
     mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
     x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    ws = make_ws(torch, tql, M, K, N, bits, 0)
+    ws = make_ws(torch, tql, M, K, N, bits, thr)
     for _ in range(reps):
-        call_linear(tql, x, M, mat, y, 0, ws, tql.EXL3_F16)
+        call_linear(tql, x, M, mat, y, thr, ws, tql.EXL3_F16)
     torch.cuda.synchronize()
 
 

@@ -116,10 +116,12 @@ int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *c
 /*
  * Workspace bytes an exl3_linear / exl3_logits_masked call with M <= M_max
  * needs on a GPU with `num_sms` streaming multiprocessors. The workspace is
- * laid out as: decode-path split-K partial sums and rotated activations;
- * then, when a prefill-shaped call is possible (m_threshold > 0 and
- * M_max >= m_threshold), the rotated activations (M_max x K fp16) and one
- * reconstruct chunk (min(n_gemm, 32768) x K fp16) ([P1] "Change": one
+ * laid out as: split-K partial sums (shared by the decode-shaped kernels
+ * and, when a prefill-shaped call is possible, the prefill GEMM's split
+ * tail tiles: at most 3 x num_sms fp32 128 x 256 tiles) and rotated
+ * activations; then, when a prefill-shaped call is possible (m_threshold > 0
+ * and M_max >= m_threshold), the rotated activations (M_max x K fp16) and
+ * one reconstruct chunk (min(n_gemm, 32768) x K fp16) ([P1] "Change": one
  * scratch per geometry, reused by every layer of that geometry on one
  * stream). Returns 0 for invalid arguments. Host only.
  */

@@ -72,15 +72,17 @@ def test_workspace_holds_one_reconstruct_chunk_within_page_bound(lib):
     chunk_bytes = K * chunk * g["bytes_per_weight"]
     assert chunk_bytes <= g["bound_mb"] * 1_000_000
     # a prefill-capable workspace for a logits-width geometry holds exactly one
-    # chunk more than a decode-shaped-only one (both hold the rotated rows)
+    # chunk more than a decode-shaped-only one (both hold the rotated rows; its
+    # decode-shaped split-K slots already exceed the prefill GEMM's tail slots)
     n_gemm, M = 248192, 2048
     with_prefill = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 128, 152)
     decode_only = tql.exl3_linear_workspace_bytes_for(M, K, n_gemm, 6, 0, 152)
     assert with_prefill - decode_only == chunk_bytes
-    # narrower than one chunk: the scratch shrinks with n_gemm (rounded to 256 rows)
+    # narrower than one chunk: the scratch shrinks with n_gemm (rounded to 256
+    # rows), plus at most the prefill GEMM's tail slots (3 x SMs fp32 128x256 tiles)
     small = tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 128, 152) - \
         tql.exl3_linear_workspace_bytes_for(M, K, 17408, 4, 0, 152)
-    assert small == 17408 * K * 2
+    assert 17408 * K * 2 <= small <= 17408 * K * 2 + 3 * 152 * 128 * 256 * 4
     # a pure 16-row decode workspace holds neither rotated rows nor a chunk
     d16 = tql.exl3_linear_workspace_bytes_for(16, K, 17408, 4, 0, 152)
     assert d16 < 32 << 20

@@ -151,6 +151,26 @@ def test_linear_prefill_path(oracle, K, N, bits, M):
     assert rel_err(y, ref) <= TOL
 
 
+@pytest.mark.parametrize("K,N,n_dec,M", [(2048, 384, 300, 6), (1024, 640, 640, 130), (4096, 256, 256, 1),
+                                         (512, 33152, 33000, 3)])
+def test_prefill_stream_k_tail(oracle, K, N, n_dec, M):
+    """Prefill-shaped calls whose tiles do not fill a wave: the tail tiles'
+    k blocks are spread over all CTAs and reduced from fp32 partial slots,
+    including a masked split tile, a last tile of only 128 columns and two
+    reconstruct chunks."""
+    bits = 4
+    m = synthetic.make_matrix(K, N, bits, seed=K + N + M)
+    x = synthetic.make_activations(M, K, seed=M + 5)
+    L = Layer(m)
+    lg, am = L.logits(to_dev(x), n_dec, 1)
+    lg = lg.cpu().numpy()
+    assert np.all(np.isneginf(lg[:, n_dec:]))
+    ref, _ = oracle.logits_masked(x, m.trellis, bits, K, N, N, n_dec, m.su, m.sv)
+    fin = np.isfinite(ref)
+    assert rel_err(lg[fin], ref[fin]) <= TOL
+    assert np.array_equal(am.cpu().numpy(), np.argmax(lg, axis=1))
+
+
 def test_tiny_workload_both_paths_and_fp16_rounding(oracle):
     t = synthetic.TINY
     m = synthetic.make_matrix(t["K"], t["N"], t["bits"], seed=t["seed"])

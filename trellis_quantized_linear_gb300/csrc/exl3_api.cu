@@ -122,6 +122,8 @@ exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const vo
     p.n_valid_local = n_valid - c0;
     p.status = dev->status;
     p.num_sms = dev->num_sms;
+    p.partials = reinterpret_cast<float *>(ws + L.partials_off);
+    p.partials_bytes = L.partials_bytes;
     e = launch_prefill_gemm(p, st);
     if (e != cudaSuccess) return EXL3_ERR_CUDA;
   }
@@ -171,6 +173,11 @@ bool workspace_layout(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_
       const size_t fb = fused_partials_bytes(L.fplan, NB);
       if (fb > pb) pb = fb;
     }
+    if (L.prefill) {  // the prefill GEMM's stream-K tail slots share the region
+      const size_t tb = prefill_tail_partials_bytes(num_sms);
+      if (tb > pb) pb = tb;
+    }
+    L.partials_bytes = pb;
     off += align_up(pb, 256);
   }
   L.xf_off = off;

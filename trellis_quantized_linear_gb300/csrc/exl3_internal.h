@@ -40,7 +40,7 @@ struct WorkspaceLayout {
   DecodePlan plan;
   FusedPlan fplan;
   bool fused = false;  // a decode-shaped call with more than 16 rows is possible
-  size_t partials_off = 0, xf_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
+  size_t partials_off = 0, partials_bytes = 0, xf_off = 0, xr_off = 0, wchunk_off = 0, total = 0;
   int64_t xr_rows = 0;      // rows of the rotated-activation buffer (multiple of 128)
   int64_t chunk_rows = 0;   // rows of the reconstruct chunk (multiple of 256)
   bool prefill = false;
@@ -77,7 +77,11 @@ struct PrefillLaunch {
   int *status;
   int num_sms;
   int rotate = 1;         // 0: plain store of x . W (weight-side rotation variant), no sv
+  float *partials = nullptr;  // fp32 slots for tail tiles split across CTAs (stream-K tail)
+  size_t partials_bytes = 0;
 };
+// Size of the stream-K tail's partial slots for any prefill GEMM launch.
+size_t prefill_tail_partials_bytes(int num_sms);
 
 struct FusedLaunch {
   const void *xr;          // rotated rows m0.. (fp16), ld = K

@@ -52,6 +52,61 @@ struct PrefillParams {
   int64_t ldy, n_valid_local;
   int M, nc, K, y_f32, tiles_m, tiles_n;
   int rotate;  // 0: the weight already carries both rotations and sv
+  // Schedule: each CTA first takes full_waves whole tiles (tile c + i * G),
+  // then its contiguous range of the tail's (tile, k block) units, U units
+  // cut evenly over the first Gsk CTAs (stream-K). A tail tile shared by
+  // several CTAs is accumulated in fp32 partial slots (128 x 256, in CTA
+  // order) that prefill_tail_finalize_kernel reduces.
+  int G, full_waves, dp_tiles, Gsk, smax;
+  int64_t U;
+  float *partials;
+};
+
+// One unit of a CTA's work: output tile, k-block range, and whether the
+// result is a partial (slot `slot` of that tail tile) or the final tile.
+struct Work {
+  int tile, kb0, kb1, slot;
+  bool partial;
+};
+
+__device__ __forceinline__ int64_t sk_owner(int64_t z, int64_t Gsk, int64_t U) { return ((z + 1) * Gsk - 1) / U; }
+
+// The CTA's work list, walked identically by the producer, MMA and epilogue.
+struct WorkIter {
+  int i;
+  int64_t u, u_end;
+  __device__ __forceinline__ void init(const PrefillParams &p) {
+    i = 0;
+    const int64_t c = blockIdx.x;
+    if (c < p.Gsk) {
+      u = c * p.U / p.Gsk;
+      u_end = (c + 1) * p.U / p.Gsk;
+    } else {
+      u = u_end = 0;
+    }
+  }
+  __device__ __forceinline__ bool next(const PrefillParams &p, int kblocks, Work &w) {
+    if (i < p.full_waves && (int)blockIdx.x + i * p.G < p.dp_tiles) {
+      w.tile = (int)blockIdx.x + i * p.G;
+      w.kb0 = 0;
+      w.kb1 = kblocks;
+      w.partial = false;
+      w.slot = 0;
+      ++i;
+      return true;
+    }
+    if (u >= u_end) return false;
+    const int64_t t = u / kblocks;
+    w.kb0 = (int)(u % kblocks);
+    const int64_t left = u_end - u;
+    w.kb1 = (int)((kblocks - w.kb0) < left ? kblocks : w.kb0 + left);
+    const int64_t first = sk_owner(t * kblocks, p.Gsk, p.U), last = sk_owner((t + 1) * kblocks - 1, p.Gsk, p.U);
+    w.tile = p.dp_tiles + (int)t;
+    w.partial = last > first;
+    w.slot = (int)((int64_t)blockIdx.x - first);
+    u += w.kb1 - w.kb0;
+    return true;
+  }
 };
 
 // In-register orthonormal had_r_128 of one row block, then * sv, mask, store
@@ -101,6 +156,9 @@ __device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillPar
   }
 }
 
+// SK = false: whole tiles 0 .. dp_tiles-1 in data-parallel waves (tile
+// c + i * gridDim.x). SK = true: only the stream-K tail (see PrefillParams).
+template <bool SK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const PrefillParams p) {
@@ -118,8 +176,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t done_bar = smem_u32(&bars[2 * STAGES + 4]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ntiles = p.tiles_m * p.tiles_n;
   const int kblocks = p.K / BK;
+  const int ntiles = p.dp_tiles;  // whole tiles of a data-parallel launch
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -143,112 +201,252 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A split tail's launch may start on SMs this launch leaves (no shared data).
+  if constexpr (!SK) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
-        tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
-        tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+    if constexpr (!SK) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
+          tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
+          tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    for (int s = 0; s < STAGES; ++s) {
-      const int64_t uses = issued / STAGES + (s < issued % STAGES ? 1 : 0);
-      if (uses > 0) mbar_wait_short(full_bar(s), (uint32_t)((uses - 1) & 1));
+      for (int s = 0; s < STAGES; ++s) {
+        const int64_t uses = issued / STAGES + (s < issued % STAGES ? 1 : 0);
+        if (uses > 0) mbar_wait_short(full_bar(s), (uint32_t)((uses - 1) & 1));
+      }
+    } else {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      WorkIter it;
+      it.init(p);
+      Work w;
+      while (ok && it.next(p, kblocks, w)) {
+        const int tm = w.tile % p.tiles_m, tn = w.tile / p.tiles_m;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
+          tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
+          tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        const int64_t uses = issued / STAGES + (s < issued % STAGES ? 1 : 0);
+        if (uses > 0) mbar_wait_short(full_bar(s), (uint32_t)((uses - 1) & 1));
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
-      if (!mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.status)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(full_bar(stage), phase, p.status)) {
-          ok = false;
-          break;
-        }
+    if constexpr (!SK) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.status)) break;
         tc_fence_after();
-        const uint64_t ad = sw128_desc(a_s(stage));
-        const uint64_t bd = sw128_desc(b_s(stage));
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // +32 bytes per 16-element K step inside the 128-byte swizzle atom
-          tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(a_s(stage));
+          const uint64_t bd = sw128_desc(b_s(stage));
+  #pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // +32 bytes per 16-element K step inside the 128-byte swizzle atom
+            tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        tc_commit(empty_bar(stage));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
       }
-      if (!ok) break;
-      tc_commit(tfull_bar(acc));
+      // All issued MMAs must finish before TMEM is released.
+      tc_commit(done_bar);
+      mbar_wait_short(done_bar, 0);
+    } else {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      WorkIter it;
+      it.init(p);
+      Work w;
+      for (; ok && it.next(p, kblocks, w); ++local) {
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(a_s(stage));
+          const uint64_t bd = sw128_desc(b_s(stage));
+  #pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // +32 bytes per 16-element K step inside the 128-byte swizzle atom
+            tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb != w.kb0 || kk != 0));
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+      }
+      // All issued MMAs must finish before TMEM is released.
+      tc_commit(done_bar);
+      mbar_wait_short(done_bar, 0);
     }
-    // All issued MMAs must finish before TMEM is released.
-    tc_commit(done_bar);
-    mbar_wait_short(done_bar, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
-    const int lg = warp & 3;  // TMEM lane group this warp may access
-    const int row_in_tile = lg * 32 + lane;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
-      const int acc = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
-      if (!mbar_wait(tfull_bar(acc), use & 1u, p.status)) break;
-      tc_fence_after();
-      const int64_t row = (int64_t)tm * BM + row_in_tile;
-      const uint32_t tbase = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * BN);
-      const int c0 = tn * BN;
-      const bool second = c0 + 128 < p.nc;
-      float v[128];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float t[32];
-        tmem_ld32(tbase + 32 * j, t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
-      }
-      if (!second) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
-      }
-      epilogue_block(v, p, row, c0);
-      if (second) {
-#pragma unroll
+    if constexpr (!SK) {
+      const int lg = warp & 3;  // TMEM lane group this warp may access
+      const int row_in_tile = lg * 32 + lane;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(tfull_bar(acc), use & 1u, p.status)) break;
+        tc_fence_after();
+        const int64_t row = (int64_t)tm * BM + row_in_tile;
+        const uint32_t tbase = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * BN);
+        const int c0 = tn * BN;
+        const bool second = c0 + 128 < p.nc;
+        float v[128];
+  #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float t[32];
-          tmem_ld32(tbase + 128 + 32 * j, t);
-#pragma unroll
+          tmem_ld32(tbase + 32 * j, t);
+  #pragma unroll
           for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
         }
+        if (!second) {
           tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
-        epilogue_block(v, p, row, c0 + 128);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        epilogue_block(v, p, row, c0);
+        if (second) {
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float t[32];
+            tmem_ld32(tbase + 128 + 32 * j, t);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
+          }
+            tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          epilogue_block(v, p, row, c0 + 128);
+        }
+      }
+    } else {
+      const int lg = warp & 3;  // TMEM lane group this warp may access
+      const int row_in_tile = lg * 32 + lane;
+      int local = 0;
+      WorkIter it;
+      it.init(p);
+      Work w;
+      for (; it.next(p, kblocks, w); ++local) {
+        const int tm = w.tile % p.tiles_m, tn = w.tile / p.tiles_m;
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(tfull_bar(acc), use & 1u, p.status)) break;
+        tc_fence_after();
+        const int64_t row = (int64_t)tm * BM + row_in_tile;
+        const uint32_t tbase = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * BN);
+        const int c0 = tn * BN;
+        const bool second = c0 + 128 < p.nc;
+        if (w.partial) {
+          // This CTA's share of a tail tile: fp32 partial sums, row-major 128 x 256.
+          float *slot = p.partials + ((int64_t)(w.tile - p.dp_tiles) * p.smax + w.slot) * (BM * BN) +
+                        (int64_t)row_in_tile * BN;
+          const int ncols = second ? BN : 128;
+          for (int j = 0; j < ncols; j += 32) {
+            float t[32];
+            tmem_ld32(tbase + j, t);
+            if (row < p.M) {
+              float4 *dst = reinterpret_cast<float4 *>(slot + j);
+  #pragma unroll
+              for (int a = 0; a < 8; ++a) dst[a] = make_float4(t[4 * a], t[4 * a + 1], t[4 * a + 2], t[4 * a + 3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          continue;
+        }
+        float v[128];
+  #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float t[32];
+          tmem_ld32(tbase + 32 * j, t);
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
+        }
+        if (!second) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        epilogue_block(v, p, row, c0);
+        if (second) {
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float t[32];
+            tmem_ld32(tbase + 128 + 32 * j, t);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 * j + i] = t[i];
+          }
+            tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          epilogue_block(v, p, row, c0 + 128);
+        }
       }
     }
   }
@@ -259,6 +457,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
+  }
+  // Launched as a programmatic dependent of the whole-tile launch: finish
+  // only after it, so that work queued behind this launch sees both done.
+  if constexpr (SK) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Reduces the partial slots of every tail tile shared by several CTAs, in
+// CTA order, then applies the epilogue (had_r_128 per 128-column block, sv,
+// mask) and stores y. One warp per (tail tile, row); lane l holds the eight
+// columns 128*(l/16) + 8*(l%16) .. +7 of the tile's 256.
+__global__ void __launch_bounds__(256) prefill_tail_finalize_kernel(const PrefillParams p, int kblocks) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wi = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t t = wi >> 7;
+  const int r = (int)(wi & 127);
+  const int64_t tail = (int64_t)p.tiles_m * p.tiles_n - p.dp_tiles;
+  if (t >= tail) return;
+  const int64_t first = sk_owner(t * kblocks, p.Gsk, p.U), last = sk_owner((t + 1) * kblocks - 1, p.Gsk, p.U);
+  if (last == first) return;  // finished by its single CTA
+  const int tile = p.dp_tiles + (int)t;
+  const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+  const int64_t row = (int64_t)tm * BM + r;
+  if (row >= p.M) return;
+  const int c0 = tn * BN, half = lane >> 4, l16 = lane & 15;
+  const bool second = c0 + 128 < p.nc;
+  const float *src = p.partials + t * p.smax * (int64_t)(BM * BN) + (int64_t)r * BN + 128 * half + 8 * l16;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int cnt = (int)(last - first + 1);
+  for (int s = 0; s < cnt; ++s) {  // slot (CTA) order
+    if (half == 0 || second) {
+      const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)s * (BM * BN)));
+      const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)s * (BM * BN)) + 1);
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+      v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    }
+  }
+  const int col0 = c0 + 128 * half + 8 * l16;
+  if (p.rotate) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!(i & h)) {
+          const float a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
+        v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
+      }
+    if (half == 1 && !second) return;
+    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.sv + col0));
+    const __half *h = reinterpret_cast<const __half *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      v[i] = (col0 + i < p.n_valid_local) ? v[i] * (__half2float(h[i]) * kInvSqrt128) : -INFINITY;
+  } else if (half == 1 && !second) {
+    return;
+  }
+  if (p.y_f32) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + row * p.ldy + col0);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    uint32_t wv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __half2 h2 = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+      wv[e] = *reinterpret_cast<uint32_t *>(&h2);
+    }
+    *reinterpret_cast<uint4 *>(static_cast<__half *>(p.y) + row * p.ldy + col0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
 }
 
@@ -297,8 +570,16 @@ cudaError_t init_prefill_kernels() {
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  return cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, prefill_tail_finalize_kernel);
 }
+
+size_t prefill_tail_partials_bytes(int num_sms) { return (size_t)3 * num_sms * BM * BN * 4; }
 
 cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   if (L.M == 0 || L.nc == 0) return cudaSuccess;
@@ -319,8 +600,71 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   p.tiles_m = (int)ceil_div(L.M, BM);
   p.tiles_n = (int)ceil_div(L.nc, BN);
   const int ntiles = p.tiles_m * p.tiles_n;
-  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
-  prefill_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
+  const int kblocks = p.K / BK;
+  // Data-parallel waves of whole tiles, then the remaining tiles' k blocks
+  // spread evenly over the CTAs (at least 4 k blocks each); see PrefillParams.
+  p.G = L.num_sms;
+  p.full_waves = ntiles / p.G;
+  p.dp_tiles = p.full_waves * p.G;
+  const int64_t tail = ntiles - p.dp_tiles;
+  p.U = tail * kblocks;
+  p.Gsk = 0;
+  p.smax = 1;
+  p.partials = L.partials;
+  // Splitting the tail pays off when it fills at most half a wave and either
+  // the whole problem is small (the split multiplies the CTAs at work) or K
+  // is long (each saved round is expensive). Otherwise the split tiles'
+  // fp32 partials and the lost lockstep of CTAs that share weight columns
+  // (re-read from HBM when the chunk exceeds L2) cost more than the idle
+  // SMs of the last wave (measured on the 4-bit MLP geometries).
+  const bool split_tail = p.U > 0 && 2 * tail <= p.G && (2 * ntiles <= p.G || kblocks >= 128);
+  if (p.U > 0 && !split_tail) {
+    p.full_waves += 1;
+    p.dp_tiles = ntiles;
+    p.U = 0;
+  }
+  if (p.U > 0) {
+    int64_t gsk = p.U / 4;
+    if (gsk < 1) gsk = 1;
+    if (gsk > p.G) gsk = p.G;
+    int64_t smax = 1;
+    for (int64_t t = 0; t < tail; ++t) {
+      const int64_t c = (((t + 1) * kblocks) * gsk - 1) / p.U - (((t * kblocks + 1) * gsk - 1) / p.U) + 1;
+      if (c > smax) smax = c;
+    }
+    if (L.partials != nullptr && (size_t)(tail * smax) * BM * BN * 4 <= L.partials_bytes) {
+      p.Gsk = (int)gsk;
+      p.smax = (int)smax;
+    } else {  // no room for partial slots: the tail runs as one more wave of whole tiles
+      p.full_waves += 1;
+      p.dp_tiles = ntiles;
+      p.U = 0;
+    }
+  }
+  // Whole tiles first (data-parallel waves), then, when the tail is split, a
+  // second launch that spreads the tail's k blocks over Gsk CTAs.
+  if (p.dp_tiles > 0) {
+    prefill_gemm_kernel<false><<<p.dp_tiles < p.G ? p.dp_tiles : p.G, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (p.Gsk == 0) return cudaSuccess;
+  PrefillParams q = p;
+  q.full_waves = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.Gsk);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.dp_tiles > 0 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<true>, ma, mb, q);
+  if (e != cudaSuccess) return e;
+  const int64_t warps = tail * BM;
+  prefill_tail_finalize_kernel<<<(unsigned)ceil_div(warps, 8), 256, 0, st>>>(q, kblocks);
   return cudaGetLastError();
 }
 
