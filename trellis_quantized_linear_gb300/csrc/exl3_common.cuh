@@ -130,18 +130,45 @@ __device__ __forceinline__ uint32_t decode_pair_sel(uint32_t state_a, uint32_t s
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// Weight of one state in both halves of a half2: one fp16 add of the masked
+// word's halves (operands selected by half). An mma A register holding
+// {w, w} against a B register holding {x, 0} contributes exactly w * x, so
+// no packing of two weights into one register is needed.
+__device__ __forceinline__ uint32_t decode_dup(uint32_t state) {
+  const uint32_t u = lcg_word(state);
+  const __half2 h = *reinterpret_cast<const __half2 *>(&u);
+  const __half2 r = __hadd2(__low2half2(h), __high2half2(h));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // Window states of a lane's four rows; for BITS = 4 a nibble-shifted copy
 // of the words makes every state one instruction.
-template <int BITS>
+//
+// kFma (BITS = 4 only) moves work from the half-rate integer ALU pipe to
+// the FMA pipe: 1: the nibble-shifted copy is x * 16 (only bits 4..31 of a
+// shifted word are ever read, so the low nibble needs no bits from the
+// next word); 2: also the states at bit offsets 0 and 4 of a word are the
+// high word of x * 65536. The multipliers m16 = 16 and m64k = 65536 must
+// come from memory the compiler cannot see (kernel parameters), or it turns
+// them back into shifts.
+template <int BITS, int kFma = 0>
 struct Windows {
   RowWindows<BITS> rw;
   uint32_t X4[4 * BITS];
-  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
+  uint32_t m64k;
+  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16 = 16u,
+                                        uint32_t m64k_ = 65536u) {
     rw.build(own, prev);
+    m64k = m64k_;
     if constexpr (BITS == 4) {
+      if constexpr (kFma) {
 #pragma unroll
-      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
-      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
+        for (int j = 0; j < 4 * BITS; ++j) X4[j] = rw.X[j] * m16;
+      } else {
+#pragma unroll
+        for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
+        X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
+      }
     }
   }
   template <int R, int C>
@@ -153,11 +180,19 @@ struct Windows {
       static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
       static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
       if constexpr (o == 0) {
-        return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
+        if constexpr (kFma >= 2 && j < 4 * BITS) {
+          return __umulhi(rw.X[j], m64k);  // seq[j], the high half of X[j]
+        } else {
+          return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
+        }
       } else if constexpr (o == 8) {
         return __byte_perm(rw.X[j], 0u, 0x4421);
       } else if constexpr (o == 4) {
-        return X4[j] >> 16;
+        if constexpr (kFma >= 2) {
+          return __umulhi(X4[j], m64k);
+        } else {
+          return X4[j] >> 16;
+        }
       } else {
         return __byte_perm(X4[j], 0u, 0x4421);
       }

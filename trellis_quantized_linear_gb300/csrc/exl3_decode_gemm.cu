@@ -21,10 +21,15 @@
 //      stage.
 //      Lane (g, q) decodes tile g, rows 4q..4q+3 straight into m16n8k16 A
 //      fragments (A = W^T: mma row r <-> output column 16*(r%8) + j +
-//      8*(r/8) for mma j; mma k index 2q, 2q+1, 2q+8, 2q+9 <-> tile rows
-//      4q..4q+3, the same permutation x' was written in), B = x'^T (8 tokens
-//      per mma). After 8 mmas per slab and token group, lane (g, q) holds
-//      output columns 16g .. 16g+15 of tokens 2q, 2q+1 (+8).
+//      8*(r/8) for mma j), B = x'^T (8 tokens per mma). Each A register
+//      holds one weight in both halves and the matching B register {x', 0}:
+//      mma k index 2q <-> tile row 4q and 2q+8 <-> row 4q+1 in the first
+//      mma of a column group, rows 4q+2 and 4q+3 in the second (odd k
+//      indices multiply zeros). This spends twice the mmas (tensor pipe
+//      ~20 % busy) to save the two instructions per weight pair that would
+//      pack two decoded weights into one register. After 16 mmas per slab
+//      and token group, lane (g, q) holds output columns 16g .. 16g+15 of
+//      tokens 2q, 2q+1 (+8).
 //      When a warp finishes its part of an n-block it either owns the whole
 //      n-block (then it applies had_r_128 over the 128 columns, sv and the
 //      -inf mask and writes y), or it stores an fp32 partial in its slot.
@@ -55,6 +60,36 @@
 #endif
 #ifndef EXL3_DECODE_PACK_FMA_M16
 #define EXL3_DECODE_PACK_FMA_M16 1
+#endif
+// A operand form, per variant (1: each weight duplicated in both halves of
+// its register against zero-interleaved x', two mmas per slab and column
+// group; 0: two weights packed per register, one mma).
+#ifndef EXL3_DECODE_DUP_M8
+#define EXL3_DECODE_DUP_M8 1
+#endif
+#ifndef EXL3_DECODE_DUP_M16
+#define EXL3_DECODE_DUP_M16 0
+#endif
+// Where the end of this warp's part of an n-block is tested, per variant
+// (1: once per chunk, after its last slab; 0: after every slab).
+#ifndef EXL3_DECODE_BLOCK_PER_CHUNK_M8
+#define EXL3_DECODE_BLOCK_PER_CHUNK_M8 1
+#endif
+#ifndef EXL3_DECODE_BLOCK_PER_CHUNK_M16
+#define EXL3_DECODE_BLOCK_PER_CHUNK_M16 0
+#endif
+// Prefetch of the next slab's x' (1: skipped past the end of the range;
+// 0: unconditional, the slab index wrapping at K).
+#ifndef EXL3_DECODE_X_COND
+#define EXL3_DECODE_X_COND 1
+#endif
+// Window extraction on the FMA pipe for BITS = 4, per variant (levels 0-2,
+// see Windows; level 2 measured 18 % slower at 1 row).
+#ifndef EXL3_DECODE_FMA_EXTRACT_M8
+#define EXL3_DECODE_FMA_EXTRACT_M8 1
+#endif
+#ifndef EXL3_DECODE_FMA_EXTRACT_M16
+#define EXL3_DECODE_FMA_EXTRACT_M16 0
 #endif
 #ifndef EXL3_DECODE_STAGES_M8
 #define EXL3_DECODE_STAGES_M8 2
@@ -100,6 +135,7 @@ struct DecodeParams {
   int *status;
   int64_t tiles_n, n_gemm, n_valid, TS, P;
   int rows, y_f32, KT, smax;
+  uint32_t m16, m64k;  // 16 and 65536, opaque to the compiler (see Windows)
 };
 
 __device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
@@ -271,58 +307,9 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
       dst[3] = v.w;
     }
   };
-  load_x(tk, bx_next);
-  int64_t z = z0;
-  while (z < z1) {
-    if (lane == 0 && zi < z1) issue_next();
-    if (!mbar_wait(smem_u32(&bars[s]), phase, p.status)) {
-      if (lane == 0) {  // let this warp's copies in flight land before it retires
-        int ws = s;
-        uint32_t wp = phase;
-        for (int64_t u = consumed; u < issued; ++u) {
-          mbar_wait_short(smem_u32(&bars[ws]), wp);
-          if (++ws == R) {
-            ws = 0;
-            wp ^= 1u;
-          }
-        }
-      }
-      return;
-    }
-    const uint8_t *stage = ring + s * Cfg::kStage;
-    const int64_t left = z1 - z;
-    const int len = (int)((KT - tk) < CHK ? ((int64_t)(KT - tk) < left ? (KT - tk) : left)
-                                          : (CHK < left ? CHK : left));
-#pragma unroll(MT == 1 ? 2 : 1)  // two slabs per iteration for <= 8 rows (measured: 1-1.5 % faster)
-    for (int i = 0; i < len; ++i) {
-    uint32_t own[2 * BITS];
-    load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
-#pragma unroll
-    for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
-    if (z + i + 1 < z1) load_x(tk + 1 == KT ? 0 : tk + 1, bx_next);
-    const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-    Windows<BITS> win;
-    win.build(own, prev);
-    static_for<8>([&](auto J) {
-      constexpr int j = J.value;
-      constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
-      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
-      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
-      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
-      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
-    });
-    const bool block_done = (tk == KT - 1) || (z + i == z1 - 1);
-    const int cur_nb = nb;
-    if (++tk == KT) {
-      tk = 0;
-      ++nb;
-    }
-    if (!block_done) continue;
-
-    // ---- this warp's part of n-block cnb is complete ----
-    const int64_t cnb = cur_nb;
+  // This warp's part of n-block cnb is complete: finish it or store the
+  // partial, then clear the accumulators.
+  auto block_end = [&](const int64_t cnb) {
     float v[MT][2][16];
     const bool whole = (z0 <= cnb * p.KT) && (z1 >= (cnb + 1) * p.KT);
     if (whole) {
@@ -360,7 +347,110 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
+  };
+  constexpr bool kPerChunk = MT == 1 ? EXL3_DECODE_BLOCK_PER_CHUNK_M8 : EXL3_DECODE_BLOCK_PER_CHUNK_M16;
+  int xk = tk;  // k slab of bx_next
+  load_x(xk, bx_next);
+  int64_t z = z0;
+  while (z < z1) {
+    if (lane == 0 && zi < z1) issue_next();
+    if (!mbar_wait(smem_u32(&bars[s]), phase, p.status)) {
+      if (lane == 0) {  // let this warp's copies in flight land before it retires
+        int ws = s;
+        uint32_t wp = phase;
+        for (int64_t u = consumed; u < issued; ++u) {
+          mbar_wait_short(smem_u32(&bars[ws]), wp);
+          if (++ws == R) {
+            ws = 0;
+            wp ^= 1u;
+          }
+        }
+      }
+      return;
+    }
+    const uint8_t *stage = ring + s * Cfg::kStage;
+    const int64_t left = z1 - z;
+    const int len = (int)((KT - tk) < CHK ? ((int64_t)(KT - tk) < left ? (KT - tk) : left)
+                                          : (CHK < left ? CHK : left));
+    // A chunk lies inside one n-block, so only its last slab can end this
+    // warp's part of an n-block (kPerChunk tests it once per chunk).
+#pragma unroll(MT == 1 ? 2 : 1)  // two slabs per iteration for <= 8 rows (measured: 1-1.5 % faster)
+    for (int i = 0; i < len; ++i) {
+    uint32_t own[2 * BITS];
+    load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
+#pragma unroll
+    for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
+    // x' of the next k slab (wrapping at K: past the end of the range this
+    // reads a valid slab that goes unused)
+    if constexpr (kPerChunk) {
+      xk = xk + 1 == KT ? 0 : xk + 1;
+    } else {
+      xk = tk + 1 == KT ? 0 : tk + 1;  // tk: this slab
+    }
+    if (!EXL3_DECODE_X_COND || z + i + 1 < z1) load_x(xk, bx_next);
+    const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
+    constexpr int kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
+    Windows<BITS, kFx> win;
+    win.build(own, prev, p.m16, p.m64k);
+    constexpr bool kDup = MT == 1 ? EXL3_DECODE_DUP_M8 : EXL3_DECODE_DUP_M16;
+    if constexpr (kDup) {
+    // B registers {x'[k], 0} for slab rows 4q .. 4q+3 of each token group.
+    uint32_t bz[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      bz[mt][0] = bx[2 * mt] & 0xFFFFu;
+      bz[mt][1] = bx[2 * mt] >> 16;
+      bz[mt][2] = bx[2 * mt + 1] & 0xFFFFu;
+      bz[mt][3] = bx[2 * mt + 1] >> 16;
+    }
+    static_for<8>([&](auto J) {
+      constexpr int j = J.value;
+      // rows 4q, 4q+1 of the lane's tile (mma k 2q and 2q+8), then 4q+2, 4q+3
+      const uint32_t a0 = decode_dup(win.template state<0, j>());
+      const uint32_t a1 = decode_dup(win.template state<0, j + 8>());
+      const uint32_t a2 = decode_dup(win.template state<1, j>());
+      const uint32_t a3 = decode_dup(win.template state<1, j + 8>());
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bz[mt][0], bz[mt][1]);
+      const uint32_t c0 = decode_dup(win.template state<2, j>());
+      const uint32_t c1 = decode_dup(win.template state<2, j + 8>());
+      const uint32_t c2 = decode_dup(win.template state<3, j>());
+      const uint32_t c3 = decode_dup(win.template state<3, j + 8>());
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], c0, c1, c2, c3, bz[mt][2], bz[mt][3]);
+    });
+    } else {
+    static_for<8>([&](auto J) {
+      constexpr int j = J.value;
+      constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
+      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
+      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
+      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
+      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
+    });
+    }
+    if constexpr (!kPerChunk) {
+      const bool done = (tk == KT - 1) || (z + i == z1 - 1);
+      const int cur_nb = nb;
+      if (++tk == KT) {
+        tk = 0;
+        ++nb;
+      }
+      if (done) block_end(cur_nb);
+    }
     }  // slabs of this chunk
+    if constexpr (kPerChunk) {
+      tk += len;
+      if (tk == KT || z + len == z1) {
+        block_end(nb);
+        if (tk == KT) {
+          tk = 0;
+          ++nb;
+        }
+      }
+    }
     __syncwarp();  // every lane has consumed this stage before lane 0 refills it
 #if EXL3_DECODE_PROXY_FENCE
     fence_proxy_async_shared();
@@ -733,6 +823,8 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   dp.P = L.plan.P[MT - 1];
   dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
+  dp.m16 = 16u;
+  dp.m64k = 65536u;
   dp.y_f32 = L.y_f32;
   const int64_t grid = L.plan.grid[MT - 1];
   cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, grid, st) : launch_mt<2>(L.bits, dp, grid, st);
