@@ -175,6 +175,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+DECODE_SOURCES = ("trellis_quantized_linear_gb300/csrc/exl3_decode_gemm.cu",
+                  "trellis_quantized_linear_gb300/csrc/exl3_common.cuh")
+
+
 def source_hash(*rel):
     h = hashlib.sha256()
     for r in rel:
@@ -183,16 +187,17 @@ def source_hash(*rel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_file: str, summary: str):
+def profiled_traffic(kernel_files, summary: str):
     """DRAM bytes per launch from a committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel's sources (its file and the device header it inlines) changed
+    since the counters were taken."""
     path = os.path.join(ROOT, "profiles", summary)
     try:
         with open(path) as f:
             text = f.read()
     except OSError:
         return None
-    want = source_hash(kernel_file)
+    want = source_hash(*kernel_files)
     rec_hash, traffic = None, None
     for line in text.splitlines():
         if line.startswith("source_sha256_16:"):
@@ -324,8 +329,7 @@ def bench_decode(args, torch, tql, peaks, dist):
         "value": value, "ms_per_step": ms_per_step, "clocks": clk, "per_m": per_m,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": profiled_traffic("trellis_quantized_linear_gb300/csrc/exl3_decode_gemm.cu",
-                                                 "decode_gemm_gate_k5120_n17408_b4.md"),
+                     "traffic": profiled_traffic(DECODE_SOURCES, "decode_gemm_gate_k5120_n17408_b4.md"),
                      "peak_kind": f"of {peaks['source']} (burst copy)", "kernel": "decode_gemm_kernel<4,*>",
                      "bytes_per_launch": wbytes},
         # each decode-shaped call launches three kernels: input rotation,
