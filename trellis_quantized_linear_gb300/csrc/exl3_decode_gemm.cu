@@ -105,6 +105,11 @@
 #ifndef EXL3_DECODE_PDL
 #define EXL3_DECODE_PDL 1
 #endif
+// The input rotation, too, as a programmatic dependent of whatever precedes
+// it in the stream (1: on).
+#ifndef EXL3_DECODE_ROTATE_PDL
+#define EXL3_DECODE_ROTATE_PDL 1
+#endif
 
 namespace exl3 {
 
@@ -222,6 +227,70 @@ __device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const Decode
 }
 
 __device__ __forceinline__ int64_t slab_owner(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
+
+// Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv,
+// mask and store of one row of n-block nb.
+__device__ __forceinline__ void finalize_row(float (&v)[4], const __half *__restrict__ sv, void *y, int y_f32,
+                                             int64_t n_gemm, int64_t n_valid, int64_t nb, int m, int lane) {
+  {
+    float a = v[0], b = v[1];
+    v[0] = a + b;
+    v[1] = a - b;
+    a = v[2];
+    b = v[3];
+    v[2] = a + b;
+    v[3] = a - b;
+    a = v[0];
+    b = v[2];
+    v[0] = a + b;
+    v[2] = a - b;
+    a = v[1];
+    b = v[3];
+    v[1] = a + b;
+    v[3] = a - b;
+  }
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
+      v[i] = (lane & s) ? (o - v[i]) : (v[i] + o);
+    }
+  const int64_t col = nb * 128 + 4 * lane;
+  const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(sv + col));
+  const __half *sh = reinterpret_cast<const __half *>(&sraw);
+  float o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = (col + i < n_valid) ? v[i] * (__half2float(sh[i]) * kInvSqrt128) : -INFINITY;
+  if (y_f32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(y) + (int64_t)m * n_gemm + col) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+    __half2 h0 = __floats2half2_rn(o[0], o[1]), h1 = __floats2half2_rn(o[2], o[3]);
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + (int64_t)m * n_gemm + col) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+  }
+}
+
+// Sum of the `cnt` partial slots at base, base + slot_elems, ... in slot
+// order (deterministic), four columns per lane; 16 loads per lane in flight.
+// The slots were written by other SMs: loads bypass L1.
+__device__ __forceinline__ void sum_slots(const float *base, int cnt, int64_t slot_elems, float (&v)[4]) {
+  v[0] = v[1] = v[2] = v[3] = 0.f;
+  for (int s0 = 0; s0 < cnt; s0 += 16) {
+    float4 f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)  // all loads of the chunk in flight at once
+      f[i] = (s0 + i < cnt) ? __ldcg(reinterpret_cast<const float4 *>(base + (s0 + i) * slot_elems))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // summed in slot order
+      v[0] += f[i].x;
+      v[1] += f[i].y;
+      v[2] += f[i].z;
+      v[3] += f[i].w;
+    }
+  }
+}
 
 // Waits until the preceding kernel in the stream has completed and its
 // memory is visible (no-op when launched without programmatic dependency).
@@ -354,7 +423,8 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
   int64_t z = z0;
   while (z < z1) {
     if (lane == 0 && zi < z1) issue_next();
-    if (!mbar_wait(smem_u32(&bars[s]), phase, p.status)) {
+    // warp-uniform outcome: a lane that gave up takes the whole warp out
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[s]), phase, p.status))) {
       if (lane == 0) {  // let this warp's copies in flight land before it retires
         int ws = s;
         uint32_t wp = phase;
@@ -464,48 +534,6 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
   }
 }
 
-// Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv,
-// mask and store of one row of n-block nb.
-__device__ __forceinline__ void finalize_row(float (&v)[4], const __half *__restrict__ sv, void *y, int y_f32,
-                                             int64_t n_gemm, int64_t n_valid, int64_t nb, int m, int lane) {
-  {
-    float a = v[0], b = v[1];
-    v[0] = a + b;
-    v[1] = a - b;
-    a = v[2];
-    b = v[3];
-    v[2] = a + b;
-    v[3] = a - b;
-    a = v[0];
-    b = v[2];
-    v[0] = a + b;
-    v[2] = a - b;
-    a = v[1];
-    b = v[3];
-    v[1] = a + b;
-    v[3] = a - b;
-  }
-#pragma unroll
-  for (int s = 1; s < 32; s <<= 1)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
-      v[i] = (lane & s) ? (o - v[i]) : (v[i] + o);
-    }
-  const int64_t col = nb * 128 + 4 * lane;
-  const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(sv + col));
-  const __half *sh = reinterpret_cast<const __half *>(&sraw);
-  float o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = (col + i < n_valid) ? v[i] * (__half2float(sh[i]) * kInvSqrt128) : -INFINITY;
-  if (y_f32) {
-    *reinterpret_cast<float4 *>(static_cast<float *>(y) + (int64_t)m * n_gemm + col) = make_float4(o[0], o[1], o[2], o[3]);
-  } else {
-    __half2 h0 = __floats2half2_rn(o[0], o[1]), h1 = __floats2half2_rn(o[2], o[3]);
-    *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + (int64_t)m * n_gemm + col) =
-        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
-  }
-}
 
 // Sums the partial slots of every n-block shared by several warps, in slot
 // order, then applies had_r_128 over the block's 128 columns, sv and the
@@ -517,6 +545,9 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
                                                               int64_t slot_elems, const __half *__restrict__ sv,
                                                               void *y, int y_f32, int64_t n_gemm, int64_t n_valid,
                                                               int rows, int64_t P, int64_t TS, int KT, int all_blocks) {
+  // The next op's input rotation may launch now; it waits for this grid
+  // before it touches memory.
+  if (EXL3_DECODE_ROTATE_PDL) allow_next_grid();
   wait_prior_grid();  // partial slots come from the decode kernel
   const int lane = threadIdx.x & 31;
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -527,21 +558,8 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
   if (cnt == 1 && !all_blocks) return;  // finished by its single owner
   const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s0 = 0; s0 < cnt; s0 += 16) {
-    float4 f[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)  // all loads of the chunk in flight at once
-      f[i] = (s0 + i < cnt) ? __ldcg(reinterpret_cast<const float4 *>(base + (s0 + i) * slot_elems))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {  // summed in slot order
-      v[0] += f[i].x;
-      v[1] += f[i].y;
-      v[2] += f[i].z;
-      v[3] += f[i].w;
-    }
-  }
+  float v[4];
+  sum_slots(base, cnt, slot_elems, v);
   finalize_row(v, sv, y, y_f32, n_gemm, n_valid, nb, m, lane);
 }
 
@@ -556,6 +574,7 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
                                                              int rows, int64_t P, int64_t TS, int KT) {
   constexpr int SC = 4;
   const int lane = threadIdx.x & 31;
+  if (EXL3_DECODE_ROTATE_PDL) allow_next_grid();  // as in decode_finalize_kernel
   const unsigned groups = (unsigned)((rows + RPW - 1) / RPW);
   const unsigned w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nb = w / groups;
@@ -604,6 +623,10 @@ __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restri
                                                           int rows, int64_t K, __half *__restrict__ xf) {
   constexpr int CH = 4 * MT;
   allow_next_grid();
+  // When launched as a programmatic dependent of the previous kernel in the
+  // stream (only its launch latency is hidden): x may be that kernel's
+  // output, and the previous decode GEMM may still read xf.
+  wait_prior_grid();
   const int lane = threadIdx.x & 31, l16 = lane & 15;
   const int64_t KB = K / 128;
   const int64_t jobs = 8 * MT * KB;
@@ -796,15 +819,16 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   {
     const int64_t jobs = 8 * MT * (K / 128);
     int64_t grid = ceil_div(ceil_div(jobs, 2), 8);
-    if (MT == 1)
-      rotate_frag_kernel<1><<<(unsigned)grid, 256, 0, st>>>(static_cast<const __half *>(L.x),
-                                                            static_cast<const __half *>(L.su), L.rows, K,
-                                                            static_cast<__half *>(L.xf));
+    const __half *x = static_cast<const __half *>(L.x), *su = static_cast<const __half *>(L.su);
+    __half *xf = static_cast<__half *>(L.xf);
+    cudaError_t e;
+    if (EXL3_DECODE_ROTATE_PDL && MT == 1)  // (measured 0.5 us slower for 9..16 rows)
+      e = launch_dependent(rotate_frag_kernel<1>, (unsigned)grid, 256, 0, st, x, su, L.rows, K, xf);
+    else if (MT == 1)
+      rotate_frag_kernel<1><<<(unsigned)grid, 256, 0, st>>>(x, su, L.rows, K, xf);
     else
-      rotate_frag_kernel<2><<<(unsigned)grid, 256, 0, st>>>(static_cast<const __half *>(L.x),
-                                                            static_cast<const __half *>(L.su), L.rows, K,
-                                                            static_cast<__half *>(L.xf));
-    cudaError_t e = cudaGetLastError();
+      rotate_frag_kernel<2><<<(unsigned)grid, 256, 0, st>>>(x, su, L.rows, K, xf);
+    if (!(EXL3_DECODE_ROTATE_PDL && MT == 1)) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // 2. stream-K decode GEMM
