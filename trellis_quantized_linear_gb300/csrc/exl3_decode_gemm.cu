@@ -228,10 +228,19 @@ __device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const Decode
 
 __device__ __forceinline__ int64_t slab_owner(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
 
-// Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv,
-// mask and store of one row of n-block nb.
-__device__ __forceinline__ void finalize_row(float (&v)[4], const __half *__restrict__ sv, void *y, int y_f32,
-                                             int64_t n_gemm, int64_t n_valid, int64_t nb, int m, int lane) {
+// The lane's four sv values of n-block nb (columns nb*128 + 4*lane ..).
+// sv is a weight, not an output of the GEMM: a kernel that waits for the
+// GEMM loads it before the wait, off the critical path (after a long decode
+// it has usually left L2).
+__device__ __forceinline__ uint2 load_sv4(const __half *__restrict__ sv, int64_t nb, int lane) {
+  return __ldg(reinterpret_cast<const uint2 *>(sv + nb * 128 + 4 * lane));
+}
+
+// Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv
+// (the lane's four values from load_sv4), mask and store of one row of
+// n-block nb.
+__device__ __forceinline__ void finalize_row(float (&v)[4], uint2 sraw, void *y, int y_f32, int64_t n_gemm,
+                                             int64_t n_valid, int64_t nb, int m, int lane) {
   {
     float a = v[0], b = v[1];
     v[0] = a + b;
@@ -257,7 +266,6 @@ __device__ __forceinline__ void finalize_row(float (&v)[4], const __half *__rest
       v[i] = (lane & s) ? (o - v[i]) : (v[i] + o);
     }
   const int64_t col = nb * 128 + 4 * lane;
-  const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(sv + col));
   const __half *sh = reinterpret_cast<const __half *>(&sraw);
   float o[4];
 #pragma unroll
@@ -548,7 +556,6 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   // The next op's input rotation may launch now; it waits for this grid
   // before it touches memory.
   if (EXL3_DECODE_ROTATE_PDL) allow_next_grid();
-  wait_prior_grid();  // partial slots come from the decode kernel
   const int lane = threadIdx.x & 31;
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nb = w / rows;
@@ -557,10 +564,12 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   const int64_t pf = slab_owner(nb * KT, P, TS);
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
   if (cnt == 1 && !all_blocks) return;  // finished by its single owner
+  const uint2 s4 = load_sv4(sv, nb, lane);
+  wait_prior_grid();  // partial slots come from the decode kernel
   const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
   float v[4];
   sum_slots(base, cnt, slot_elems, v);
-  finalize_row(v, sv, y, y_f32, n_gemm, n_valid, nb, m, lane);
+  finalize_row(v, s4, y, y_f32, n_gemm, n_valid, nb, m, lane);
 }
 
 // The same reduction for the fused tensor-core GEMM (up to 256 rows, 2-3
@@ -582,6 +591,7 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
   if (nb >= n_gemm / 128) return;
   const int64_t pf = slab_owner(nb * KT, P, TS);
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
+  const uint2 s4 = load_sv4(sv, nb, lane);
   wait_prior_grid();  // partial slots come from the GEMM kernel
   const float *base = partials + nb * smax * slot_elems + (int64_t)m0 * 128 + 4 * lane;
   const int nr = rows - m0 < RPW ? rows - m0 : RPW;
@@ -610,7 +620,7 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
   }
 #pragma unroll
   for (int r = 0; r < RPW; ++r)
-    if (r < nr) finalize_row(v[r], sv, y, y_f32, n_gemm, n_valid, nb, m0 + r, lane);
+    if (r < nr) finalize_row(v[r], s4, y, y_f32, n_gemm, n_valid, nb, m0 + r, lane);
 }
 
 // x' = RNE_fp16(had_r_128(x * su)) for up to 8*MT rows, in fragment order:
@@ -801,7 +811,10 @@ cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t 
                                    int units_per_block, int all_blocks, cudaStream_t st) {
   if (!all_blocks) {
     const int64_t warps = (n_gemm / 128) * rows;
-    return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, 8), 256u, (size_t)0, st, partials,
+    // One warp per CTA for <= 8 rows spreads the slot loads over more SMs
+    // (0.35 us less at 1 row; 9..16 rows measured 0.15 us slower).
+    const unsigned wpc = rows <= 8 ? 1u : 8u;
+    return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, (int64_t)wpc), 32u * wpc, (size_t)0, st, partials,
                             smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
                             units_per_block, all_blocks);
   }
