@@ -105,6 +105,10 @@
 #ifndef EXL3_DECODE_PDL
 #define EXL3_DECODE_PDL 1
 #endif
+// Most rows for which the slot reduction runs one warp per CTA.
+#ifndef EXL3_DECODE_FIN_1W_ROWS
+#define EXL3_DECODE_FIN_1W_ROWS 2
+#endif
 // The input rotation, too, as a programmatic dependent of whatever precedes
 // it in the stream (1: on).
 #ifndef EXL3_DECODE_ROTATE_PDL
@@ -811,9 +815,9 @@ cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t 
                                    int units_per_block, int all_blocks, cudaStream_t st) {
   if (!all_blocks) {
     const int64_t warps = (n_gemm / 128) * rows;
-    // One warp per CTA for <= 8 rows spreads the slot loads over more SMs
-    // (0.35 us less at 1 row; 9..16 rows measured 0.15 us slower).
-    const unsigned wpc = rows <= 8 ? 1u : 8u;
+    // One warp per CTA for few rows spreads the slot loads over more SMs
+    // (0.35 us less at 1 row, 0.1 us at 2; 4 rows measured 0.1 us slower).
+    const unsigned wpc = rows <= EXL3_DECODE_FIN_1W_ROWS ? 1u : 8u;
     return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, (int64_t)wpc), 32u * wpc, (size_t)0, st, partials,
                             smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
                             units_per_block, all_blocks);
