@@ -341,37 +341,76 @@ def bench_decode(args, torch, tql, peaks, dist):
 
 
 def bench_e2e(args, torch, tql, state):
-    """Same metric through the public API with host buffers: per call, H2D of
-    x from pinned memory, exl3_linear, D2H of y into pinned memory; the step
-    ends with the result on the host."""
+    """Same metric through the public API with host buffers: per step, one
+    H2D of every call's x from pinned memory, the exl3_linear calls, one D2H
+    of every y into pinned memory; the step ends with the results on the
+    host. Timed two ways: the step captured once
+    in CUDA graphs (copies and calls as graph nodes, replayed; how a serving
+    loop would issue it, the headline) and issued eagerly from Python (bound
+    by host launch overhead)."""
     g = synthetic.GATE_DECODE
     K, N, Ms = g["K"], g["N"], g["Ms"]
     mats, ws = state["mats"], state["ws"]
-    hx = {M: torch.from_numpy(synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"])).pin_memory()
-          for M in Ms}
-    hy = {M: torch.empty((M, N), dtype=torch.float16).pin_memory() for M in Ms}
-    dx = {M: torch.empty((M, K), dtype=torch.float16, device="cuda") for M in Ms}
-    dy = {M: torch.empty((M, N), dtype=torch.float16, device="cuda") for M in Ms}
-    h2d = sum(hx[M].numel() * 2 for M in Ms)
-    d2h = sum(hy[M].numel() * 2 for M in Ms)
+    # the step's inputs (and outputs) for all its calls in one pinned host
+    # buffer each: one copy up and one copy down per step
+    rows = sum(Ms)
+    hx = torch.cat([torch.from_numpy(synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"]))
+                    for M in Ms]).pin_memory()
+    hy = torch.empty((rows, N), dtype=torch.float16).pin_memory()
+    dx = torch.empty((rows, K), dtype=torch.float16, device="cuda")
+    dy = torch.empty((rows, N), dtype=torch.float16, device="cuda")
+    offs = [sum(Ms[:j]) for j in range(len(Ms))]
+    h2d = hx.numel() * 2
+    d2h = hy.numel() * 2
     steps = max(20, min(args.steps // 20, 2000))
 
-    def step(i):
+    def issue(i):
+        dx.copy_(hx, non_blocking=True)
         for j, M in enumerate(Ms):
-            dx[M].copy_(hx[M], non_blocking=True)
-            call_linear(tql, dx[M], M, mats[(i * len(Ms) + j) % len(mats)], dy[M], 128, ws, tql.EXL3_F16)
-            hy[M].copy_(dy[M], non_blocking=True)
+            o = offs[j]
+            call_linear(tql, dx[o:o + M], M, mats[(i * len(Ms) + j) % len(mats)], dy[o:o + M], 128, ws,
+                        tql.EXL3_F16)
+        hy.copy_(dy, non_blocking=True)
+
+    def step(i):
+        issue(i)
         torch.cuda.current_stream().synchronize()
 
-    for i in range(10):
-        step(i)
-    t0 = time.perf_counter()
-    for i in range(steps):
-        step(i)
-    dt = (time.perf_counter() - t0) / steps
-    return {"value": round(state["weights_per_step_bytes"] / dt / 1e9, 1), "unit": "GB/s",
+    def timed(fn):
+        for i in range(10):
+            fn(i)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            fn(i)
+        return (time.perf_counter() - t0) / steps
+
+    dt_eager = timed(step)
+    # one graph per group of len(Ms) weight copies, so that consecutive steps
+    # still stream different weights (the copies exceed L2 together)
+    ngraphs = max(1, len(mats) // len(Ms))
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for k in range(ngraphs):
+            issue(k)
+        stream.synchronize()
+        for k in range(ngraphs):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                issue(k)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+
+    def gstep(i):
+        graphs[i % ngraphs].replay()
+        torch.cuda.current_stream().synchronize()
+
+    dt = timed(gstep)
+    wb = state["weights_per_step_bytes"]
+    return {"value": round(wb / dt / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4),
-            "steps": steps}
+            "steps": steps, "mode": "cuda_graph (step captured once: copies + calls, replayed)",
+            "eager": {"value": round(wb / dt_eager / 1e9, 1), "ms_per_step": round(dt_eager * 1e3, 4)}}
 
 
 # ---------------------------------------------------------------------------
