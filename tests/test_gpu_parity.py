@@ -103,7 +103,7 @@ DECODE, PREFILL = 0, 1  # m_threshold values that force each path
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (128, 256, 3), (640, 384, 6), (256, 768, 2),
                                       (384, 256, 5), (256, 256, 8), (256, 384, 1), (384, 384, 7)])
-@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 37])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 16, 37])
 def test_linear_decode_path(oracle, K, N, bits, M):
     m = synthetic.make_matrix(K, N, bits, seed=K + N + bits)
     x = synthetic.make_activations(M, K, seed=M)
