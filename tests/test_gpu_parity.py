@@ -31,7 +31,8 @@ def gpu():
 # input rotation
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 640), (256, 5120)])
+# (2048, 5120) is the prefill-shaped gate input; (700, 3840) a ragged large one.
+@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 640), (256, 5120), (2048, 5120), (700, 3840)])
 @pytest.mark.parametrize("with_scale", [True, False])
 def test_hadamard128_bit_exact(oracle, rows, cols, with_scale):
     torch = torch_mod()
@@ -46,13 +47,15 @@ def test_hadamard128_bit_exact(oracle, rows, cols, with_scale):
     assert np.array_equal(got, ref)
 
 
-def test_hadamard128_in_place(oracle):
+@pytest.mark.parametrize("rows,cols", [(9, 384), (700, 3840)])
+def test_hadamard128_in_place(oracle, rows, cols):
     torch = torch_mod()
-    x = synthetic.make_activations(9, 384, seed=3)
+    x = synthetic.make_activations(rows, cols, seed=3)
     xd = to_dev(x)
     tql.exl3_hadamard128(xd, xd, None)
     torch.cuda.synchronize()
     assert np.array_equal(xd.cpu().numpy().view(np.uint16), oracle.input_rotation(x).view(np.uint16))
+    assert tql.exl3_get_device_status() == 0
 
 
 # ---------------------------------------------------------------------------
