@@ -144,22 +144,18 @@ __device__ __forceinline__ uint32_t decode_dup(uint32_t state) {
 // Window states of a lane's four rows; for BITS = 4 a nibble-shifted copy
 // of the words makes every state one instruction.
 //
-// kFma (BITS = 4 only) moves work from the half-rate integer ALU pipe to
-// the FMA pipe: 1: the nibble-shifted copy is x * 16 (only bits 4..31 of a
-// shifted word are ever read, so the low nibble needs no bits from the
-// next word); 2: also the states at bit offsets 0 and 4 of a word are the
-// high word of x * 65536. The multipliers m16 = 16 and m64k = 65536 must
-// come from memory the compiler cannot see (kernel parameters), or it turns
-// them back into shifts.
-template <int BITS, int kFma = 0>
+// kFma (BITS = 4 only) builds the nibble-shifted copy as x * 16 on the FMA
+// pipe instead of a funnel shift on the half-rate integer ALU pipe (only
+// bits 4..31 of a shifted word are ever read, so the low nibble needs no
+// bits from the next word). The multiplier m16 = 16 must come from memory
+// the compiler cannot see (a kernel parameter), or it turns it back into a
+// shift.
+template <int BITS, bool kFma = false>
 struct Windows {
   RowWindows<BITS> rw;
   uint32_t X4[4 * BITS];
-  uint32_t m64k;
-  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16 = 16u,
-                                        uint32_t m64k_ = 65536u) {
+  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16 = 16u) {
     rw.build(own, prev);
-    m64k = m64k_;
     if constexpr (BITS == 4) {
       if constexpr (kFma) {
 #pragma unroll
@@ -180,19 +176,11 @@ struct Windows {
       static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
       static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
       if constexpr (o == 0) {
-        if constexpr (kFma >= 2 && j < 4 * BITS) {
-          return __umulhi(rw.X[j], m64k);  // seq[j], the high half of X[j]
-        } else {
-          return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
-        }
+        return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
       } else if constexpr (o == 8) {
         return __byte_perm(rw.X[j], 0u, 0x4421);
       } else if constexpr (o == 4) {
-        if constexpr (kFma >= 2) {
-          return __umulhi(X4[j], m64k);
-        } else {
-          return X4[j] >> 16;
-        }
+        return X4[j] >> 16;
       } else {
         return __byte_perm(X4[j], 0u, 0x4421);
       }

@@ -78,13 +78,9 @@
 #ifndef EXL3_DECODE_BLOCK_PER_CHUNK_M16
 #define EXL3_DECODE_BLOCK_PER_CHUNK_M16 0
 #endif
-// Prefetch of the next slab's x' (1: skipped past the end of the range;
-// 0: unconditional, the slab index wrapping at K).
-#ifndef EXL3_DECODE_X_COND
-#define EXL3_DECODE_X_COND 1
-#endif
-// Window extraction on the FMA pipe for BITS = 4, per variant (levels 0-2,
-// see Windows; level 2 measured 18 % slower at 1 row).
+// Nibble-shifted window copy made on the FMA pipe for BITS = 4 (see
+// Windows; 1: on). Also taking the offset-0 and offset-4 states from the
+// high word of a multiply (IMAD.HI) measured 18 % slower at 1 row.
 #ifndef EXL3_DECODE_FMA_EXTRACT_M8
 #define EXL3_DECODE_FMA_EXTRACT_M8 1
 #endif
@@ -144,7 +140,7 @@ struct DecodeParams {
   int *status;
   int64_t tiles_n, n_gemm, n_valid, TS, P;
   int rows, y_f32, KT, smax;
-  uint32_t m16, m64k;  // 16 and 65536, opaque to the compiler (see Windows)
+  uint32_t m16;  // 16, opaque to the compiler (see Windows)
 };
 
 __device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
@@ -462,18 +458,17 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
 #pragma unroll
     for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
-    // x' of the next k slab (wrapping at K: past the end of the range this
-    // reads a valid slab that goes unused)
+    // x' of the next k slab (none past the end of this warp's range)
     if constexpr (kPerChunk) {
       xk = xk + 1 == KT ? 0 : xk + 1;
     } else {
       xk = tk + 1 == KT ? 0 : tk + 1;  // tk: this slab
     }
-    if (!EXL3_DECODE_X_COND || z + i + 1 < z1) load_x(xk, bx_next);
+    if (z + i + 1 < z1) load_x(xk, bx_next);
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-    constexpr int kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
+    constexpr bool kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
     Windows<BITS, kFx> win;
-    win.build(own, prev, p.m16, p.m64k);
+    win.build(own, prev, p.m16);
     constexpr bool kDup = MT == 1 ? EXL3_DECODE_DUP_M8 : EXL3_DECODE_DUP_M16;
     if constexpr (kDup) {
     // B registers {x'[k], 0} for slab rows 4q .. 4q+3 of each token group.
@@ -865,7 +860,6 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
   dp.m16 = 16u;
-  dp.m64k = 65536u;
   dp.y_f32 = L.y_f32;
   const int64_t grid = L.plan.grid[MT - 1];
   cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, grid, st) : launch_mt<2>(L.bits, dp, grid, st);
