@@ -87,6 +87,15 @@
 #ifndef EXL3_DECODE_FMA_EXTRACT_M16
 #define EXL3_DECODE_FMA_EXTRACT_M16 0
 #endif
+// Slabs per inner-loop iteration, per variant (for <= 8 rows two measured
+// 1-1.5 % faster than one and 3 % faster than four; for 9..16 rows two
+// spills and is 2 % slower than one).
+#ifndef EXL3_DECODE_UNROLL_M8
+#define EXL3_DECODE_UNROLL_M8 2
+#endif
+#ifndef EXL3_DECODE_UNROLL_M16
+#define EXL3_DECODE_UNROLL_M16 1
+#endif
 #ifndef EXL3_DECODE_STAGES_M8
 #define EXL3_DECODE_STAGES_M8 2
 #endif
@@ -452,7 +461,8 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
                                           : (CHK < left ? CHK : left));
     // A chunk lies inside one n-block, so only its last slab can end this
     // warp's part of an n-block (kPerChunk tests it once per chunk).
-#pragma unroll(MT == 1 ? 2 : 1)  // two slabs per iteration for <= 8 rows (measured: 1-1.5 % faster)
+    constexpr int kUnroll = MT == 1 ? EXL3_DECODE_UNROLL_M8 : EXL3_DECODE_UNROLL_M16;
+#pragma unroll(kUnroll)
     for (int i = 0; i < len; ++i) {
     uint32_t own[2 * BITS];
     load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
