@@ -464,69 +464,69 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     constexpr int kUnroll = MT == 1 ? EXL3_DECODE_UNROLL_M8 : EXL3_DECODE_UNROLL_M16;
 #pragma unroll(kUnroll)
     for (int i = 0; i < len; ++i) {
-    uint32_t own[2 * BITS];
-    load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
+      uint32_t own[2 * BITS];
+      load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
 #pragma unroll
-    for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
-    // x' of the next k slab (none past the end of this warp's range)
-    if constexpr (kPerChunk) {
-      xk = xk + 1 == KT ? 0 : xk + 1;
-    } else {
-      xk = tk + 1 == KT ? 0 : tk + 1;  // tk: this slab
-    }
-    if (z + i + 1 < z1) load_x(xk, bx_next);
-    const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-    constexpr bool kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
-    Windows<BITS, kFx> win;
-    win.build(own, prev, p.m16);
-    constexpr bool kDup = MT == 1 ? EXL3_DECODE_DUP_M8 : EXL3_DECODE_DUP_M16;
-    if constexpr (kDup) {
-    // B registers {x'[k], 0} for slab rows 4q .. 4q+3 of each token group.
-    uint32_t bz[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      bz[mt][0] = bx[2 * mt] & 0xFFFFu;
-      bz[mt][1] = bx[2 * mt] >> 16;
-      bz[mt][2] = bx[2 * mt + 1] & 0xFFFFu;
-      bz[mt][3] = bx[2 * mt + 1] >> 16;
-    }
-    static_for<8>([&](auto J) {
-      constexpr int j = J.value;
-      // rows 4q, 4q+1 of the lane's tile (mma k 2q and 2q+8), then 4q+2, 4q+3
-      const uint32_t a0 = decode_dup(win.template state<0, j>());
-      const uint32_t a1 = decode_dup(win.template state<0, j + 8>());
-      const uint32_t a2 = decode_dup(win.template state<1, j>());
-      const uint32_t a3 = decode_dup(win.template state<1, j + 8>());
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bz[mt][0], bz[mt][1]);
-      const uint32_t c0 = decode_dup(win.template state<2, j>());
-      const uint32_t c1 = decode_dup(win.template state<2, j + 8>());
-      const uint32_t c2 = decode_dup(win.template state<3, j>());
-      const uint32_t c3 = decode_dup(win.template state<3, j + 8>());
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], c0, c1, c2, c3, bz[mt][2], bz[mt][3]);
-    });
-    } else {
-    static_for<8>([&](auto J) {
-      constexpr int j = J.value;
-      constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
-      const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
-      const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
-      const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
-      const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
-    });
-    }
-    if constexpr (!kPerChunk) {
-      const bool done = (tk == KT - 1) || (z + i == z1 - 1);
-      const int cur_nb = nb;
-      if (++tk == KT) {
-        tk = 0;
-        ++nb;
+      for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
+      // x' of the next k slab (none past the end of this warp's range)
+      if constexpr (kPerChunk) {
+        xk = xk + 1 == KT ? 0 : xk + 1;
+      } else {
+        xk = tk + 1 == KT ? 0 : tk + 1;  // tk: this slab
       }
-      if (done) block_end(cur_nb);
-    }
+      if (z + i + 1 < z1) load_x(xk, bx_next);
+      const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
+      constexpr bool kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
+      Windows<BITS, kFx> win;
+      win.build(own, prev, p.m16);
+      constexpr bool kDup = MT == 1 ? EXL3_DECODE_DUP_M8 : EXL3_DECODE_DUP_M16;
+      if constexpr (kDup) {
+        // B registers {x'[k], 0} for slab rows 4q .. 4q+3 of each token group.
+        uint32_t bz[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          bz[mt][0] = bx[2 * mt] & 0xFFFFu;
+          bz[mt][1] = bx[2 * mt] >> 16;
+          bz[mt][2] = bx[2 * mt + 1] & 0xFFFFu;
+          bz[mt][3] = bx[2 * mt + 1] >> 16;
+        }
+        static_for<8>([&](auto J) {
+          constexpr int j = J.value;
+          // rows 4q, 4q+1 of the lane's tile (mma k 2q and 2q+8), then 4q+2, 4q+3
+          const uint32_t a0 = decode_dup(win.template state<0, j>());
+          const uint32_t a1 = decode_dup(win.template state<0, j + 8>());
+          const uint32_t a2 = decode_dup(win.template state<1, j>());
+          const uint32_t a3 = decode_dup(win.template state<1, j + 8>());
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bz[mt][0], bz[mt][1]);
+          const uint32_t c0 = decode_dup(win.template state<2, j>());
+          const uint32_t c1 = decode_dup(win.template state<2, j + 8>());
+          const uint32_t c2 = decode_dup(win.template state<3, j>());
+          const uint32_t c3 = decode_dup(win.template state<3, j + 8>());
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], c0, c1, c2, c3, bz[mt][2], bz[mt][3]);
+        });
+      } else {
+        static_for<8>([&](auto J) {
+          constexpr int j = J.value;
+          constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
+          const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
+          const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
+          const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
+          const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
+        });
+      }
+      if constexpr (!kPerChunk) {
+        const bool done = (tk == KT - 1) || (z + i == z1 - 1);
+        const int cur_nb = nb;
+        if (++tk == KT) {
+          tk = 0;
+          ++nb;
+        }
+        if (done) block_end(cur_nb);
+      }
     }  // slabs of this chunk
     if constexpr (kPerChunk) {
       tk += len;
