@@ -213,8 +213,8 @@ exl3_status exl3_linear_weight_rotated(const void *x, int64_t M, int64_t K, cons
  *          Otherwise the prefill-shaped path runs had_r_128 -> reconstruct
  *          (32768-column chunks into the workspace) -> tensor-core GEMM with
  *          the output rotation fused in its epilogue. On one GB300 the
- *          prefill-shaped path becomes faster between M = 384 and M = 1024
- *          depending on the shape (both 4-bit MLP shapes measured).
+ *          prefill-shaped path is faster from M = 768 (4-bit 5120 -> 17408)
+ *          and from M = 1024 (4-bit 17408 -> 5120).
  *   workspace: device buffer of at least
  *          exl3_linear_workspace_bytes(M, K, n_gemm, bits, m_threshold)
  *          bytes, cleared once by exl3_workspace_init. Calls that share a
