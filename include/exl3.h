@@ -42,6 +42,13 @@
  *     current, before any other call that touches it and before any CUDA
  *     graph capture: it loads every kernel and sets their attributes, so
  *     no later call loads modules, allocates or queries the device.
+ *   - Consecutive kernels of one call overlap their launches through
+ *     programmatic dependent launch; each waits for its predecessor before
+ *     touching memory it shares with it. The last kernel of a call lets the
+ *     next kernel in the stream begin early as well: a caller kernel that
+ *     opts into programmatic stream serialization must, as that contract
+ *     requires, wait on its grid dependency (cudaGridDependencySynchronize)
+ *     before reading this call's outputs. Ordinary launches are unaffected.
  *   - Supported trellis widths: bits in 1..8.
  *   - Shapes: K % 128 == 0, K <= 131072, n_gemm % 128 == 0,
  *     n_gemm <= n_stored, n_stored % 128 == 0, n_stored <= 2^24; others
