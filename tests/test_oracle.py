@@ -7,6 +7,7 @@ of the mathematics, a second decoder, and dense brute force. None of these
 tests needs a GPU.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -372,3 +373,32 @@ def test_argmax_first_index_on_ties(oracle):
     lg = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 9.0]])
     am = oracle.mask_argmax(lg, 3)
     assert am.tolist() == [1, 0]
+
+
+def test_decode_table_matches_committed_fixture():
+    """Regression guard on the whole decode table: the oracle reproduces the
+    SHA-256 of the fp16 weights of all 65536 states, the sample states, the
+    exact-tie count (states whose half-sum lies exactly between two fp16
+    values, where only round-to-nearest-even picks the stored value) and
+    the summary statistics written to tests/golden/decode_table.txt by
+    make_decode_table.py."""
+    import importlib.util
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_decode_table", os.path.join(here, "make_decode_table.py"))
+    mk = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mk)
+    want = {}
+    samples = {}
+    for line in open(os.path.join(here, "decode_table.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, *v = line.split()
+        if k == "state":
+            samples[int(v[0], 16)] = int(v[1], 16)
+        else:
+            want[k] = v[0]
+    got = mk.table_facts()
+    assert got["sha256"] == want["sha256"]
+    assert got["samples"] == samples
+    assert got["ties"] == int(want["ties"])
+    assert got["sum"] == float(want["sum"]) and got["min"] == float(want["min"]) and got["max"] == float(want["max"])
