@@ -5,7 +5,11 @@ bits=4), one step = four exl3_linear calls at M = 1, 4, 8, 16 (fp16 in,
 fp16 out), weights resident in HBM. Metric: weight GB/s = trellis bytes read
 per step / step time. Twelve rotating weight copies (535 MB, > 4x L2) keep
 every call's weights out of L2. The timed loop replays CUDA graphs of one
-step each.
+step each. The end-to-end figure (`e2e`) times the same step through the
+public API with host buffers: one H2D of the step's inputs from pinned
+memory, the four calls, one D2H of the outputs, the whole step captured
+once as a CUDA graph and replayed (the eager, Python-issued figure is
+reported beside it).
 
 Also measured in the same run (reported as sub-objects of the JSON line):
   prefill   - the prefill-shaped call on the same geometry at M=2048
