@@ -54,6 +54,7 @@ METRIC = "EXL3 linear: decode weight GB/s, prefill TFLOP/s, both as % roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 WEIGHT_COPIES = 12
+L2_BYTES = 129 * 10**6
 
 
 # ---------------------------------------------------------------------------
@@ -257,6 +258,68 @@ def time_fn(torch, fn, iters, warmup=2):
     return s.elapsed_time(e) / iters
 
 
+def graph_time(torch, fns, reps=5, warm=2):
+    """ms per call of the closures in `fns`, captured once (in order) as one
+    CUDA graph on a side stream and replayed `warm` + `reps` times; CUDA
+    events on the replay stream bracket the timed replays."""
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for fn in fns:  # eager pass: nothing lazy happens inside the capture
+            fn()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for fn in fns:
+                fn()
+        for _ in range(warm):
+            gr.replay()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / (reps * len(fns))
+    del gr
+    return ms
+
+
+def copies_for(nbytes: int) -> int:
+    """Distinct weight copies whose calls in a row stream more than 4x the L2
+    (129 MB on GB300), at least 2."""
+    return max(2, min(WEIGHT_COPIES, -(-4 * L2_BYTES // nbytes)))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baselines for the sub-lines (test infrastructure, host cores)
+# ---------------------------------------------------------------------------
+
+def oracle_call_time(K, N, bits, M, seed, x_scale=1.0, rows=None, cols=None, matrix_index=0):
+    """Seconds the oracle takes for an M-row call of the K x N layer. With
+    `rows` (< M) the oracle runs on that many seeded rows and, with `cols`
+    (< N), on output columns [0, cols); the full-call time is then the
+    sample's time scaled by (M/rows) * (N/cols): labelled extrapolated."""
+    import oracle
+    oracle.build()
+    mat = synthetic.make_matrix(K, N, bits, seed=seed, matrix_index=matrix_index)
+    r = M if rows is None else min(rows, M)
+    c = N if cols is None else min(cols, N)
+    x = synthetic.make_activations(r, K, seed=seed, x_scale=x_scale)
+    t0 = time.perf_counter()
+    oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, c)
+    dt = time.perf_counter() - t0
+    scale = (M / r) * (N / c)
+    return {"s": dt * scale, "extrapolated": scale != 1.0, "sample": f"{r} rows x {c} columns, {dt:.2f} s",
+            "cores": oracle.num_threads()}
+
+
+def oracle_line(ms_gpu, cpu):
+    """The CPU oracle's time beside a GPU time, and their ratio."""
+    return {"oracle_ms": round(cpu["s"] * 1e3, 2), "extrapolated": cpu["extrapolated"], "sample": cpu["sample"],
+            "cores": cpu["cores"], "kind": "oracle", "gpu_speedup": round(cpu["s"] * 1e3 / ms_gpu, 1)}
+
+
 # ---------------------------------------------------------------------------
 # headline: decode-shaped gate_proj
 # ---------------------------------------------------------------------------
@@ -327,6 +390,9 @@ def bench_decode(args, torch, tql, peaks, dist):
             t_ms = time_fn(torch, gr.replay, 50, 5) / WEIGHT_COPIES
         per_m[str(M)] = {"us_per_call": round(t_ms * 1e3, 3),
                          "weight_gbs": round(wbytes / (t_ms * 1e-3) / 1e9, 1)}
+        if rank == 0 and not args.no_extras:
+            per_m[str(M)]["cpu_baseline"] = oracle_line(t_ms, oracle_call_time(K, N, bits, M, g["seed"],
+                                                                                x_scale=g["x_scale"]))
     launch_us = ms_per_step * 1e3 / len(Ms)  # the step is exactly len(Ms) decode-GEMM launches
     achieved = wbytes / (launch_us * 1e-6) / 1e9
     return {
@@ -422,66 +488,94 @@ def bench_e2e(args, torch, tql, state):
 # ---------------------------------------------------------------------------
 
 def bench_prefill(args, torch, tql, peaks):
+    """Prefill-shaped gate_proj at M=2048. Every timing replays a CUDA graph
+    of calls over distinct weight copies (more than 4x L2 in total), so each
+    call reads its trellis from HBM; the input rotation is timed over as many
+    distinct activation copies."""
     K, N, bits, M = 5120, 17408, 4, 2048
-    mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
+    nc = copies_for(K * N * bits // 8)
+    mats = [DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED, matrix_index=j))
+            for j in range(nc)]
+    mat = mats[0]
     x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     ws = make_ws(torch, tql, M, K, N, bits, 128)
-    iters = 5 if args.quick else 20
-    t_call = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 128, ws, tql.EXL3_F16), iters, 3)
+    reps = 2 if args.quick else 5
+    t_call = graph_time(torch, [lambda m=m: call_linear(tql, x, M, m, y, 128, ws, tql.EXL3_F16) for m in mats], reps)
+    xs = [x] + [torch.randn((M, K), device="cuda").half() for _ in range(nc - 1)]
     xr = torch.empty((M, K), dtype=torch.float16, device="cuda")
-    t_had = time_fn(torch, lambda: tql.exl3_hadamard128(x, xr, mat.su), iters, 2)
+    t_had = graph_time(torch, [lambda xx=xx: tql.exl3_hadamard128(xx, xr, mat.su) for xx in xs], reps)
+    del xs
     wt = torch.empty((N, K), dtype=torch.float16, device="cuda")
-    t_rec = time_fn(torch, lambda: tql.exl3_reconstruct(mat.trellis, bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK),
-                    iters, 2)
+    t_rec = graph_time(torch, [lambda m=m: tql.exl3_reconstruct(m.trellis, bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK)
+                               for m in mats], reps)
     flops = 2.0 * M * K * N
     tflops = flops / (t_call * 1e-3) / 1e12
     t_gemm = max(t_call - t_had - t_rec, 1e-6)
     peak = peaks["bf16_tflops"]  # fp16 and bf16 share the tensor-core rate
     # weight-side rotation variant on the same call: rotated reconstruct + plain GEMM
     wsr = torch.empty(tql.exl3_weight_rotated_workspace_bytes(K, N), dtype=torch.uint8, device="cuda")
-    t_wr = time_fn(torch, lambda: tql.exl3_linear_weight_rotated(x, M, K, mat.trellis, bits, N, N, mat.su, mat.sv,
-                                                                 y, tql.EXL3_F16, wsr), iters, 3)
-    t_rr = time_fn(torch, lambda: tql.exl3_reconstruct_rotated(mat.trellis, bits, K, N, 0, N, mat.su, mat.sv, wt,
-                                                               tql.EXL3_LAYOUT_NK), iters, 2)
+    t_wr = graph_time(torch, [lambda m=m: tql.exl3_linear_weight_rotated(x, M, K, m.trellis, bits, N, N, m.su, m.sv,
+                                                                         y, tql.EXL3_F16, wsr) for m in mats], reps)
+    t_rr = graph_time(torch, [lambda m=m: tql.exl3_reconstruct_rotated(m.trellis, bits, K, N, 0, N, m.su, m.sv, wt,
+                                                                       tql.EXL3_LAYOUT_NK) for m in mats], reps)
     weight_rotated = {"ms_per_call": round(t_wr, 4), "tflops": round(flops / (t_wr * 1e-3) / 1e12, 1),
                       "frac": round(flops / (t_wr * 1e-3) / 1e12 / peak, 4),
                       "reconstruct_rotated_ms": round(t_rr, 4),
                       "reconstruct_rotated_gbs": round((mat.nbytes + N * K * 2) / (t_rr * 1e-3) / 1e9, 1)}
-    del wsr
+    del wsr, mats
+    cpu = oracle_call_time(K, N, bits, M, synthetic.PREFILL_SEED, rows=128)
     return {"geometry": "K=5120 N=17408 bits=4 M=2048", "ms_per_call": round(t_call, 4),
             "weight_rotated": weight_rotated,
             "tflops": round(tflops, 1), "peak_tflops": peak, "frac": round(tflops / peak, 4),
             "peak_kind": f"of {peaks['source']} (cuBLAS bf16 burst; fp16 same rate)",
             "split_ms": {"hadamard": round(t_had, 4), "reconstruct": round(t_rec, 4), "gemm": round(t_gemm, 4)},
             "gemm_tflops": round(flops / (t_gemm * 1e-3) / 1e12, 1),
-            "reconstruct_gbs": round((mat.nbytes + N * K * 2) / (t_rec * 1e-3) / 1e9, 1)}
+            "reconstruct_gbs": round((mat.nbytes + N * K * 2) / (t_rec * 1e-3) / 1e9, 1),
+            "timing": f"CUDA graph replays over {nc} weight copies ({nc * mat.nbytes / 1e6:.0f} MB > 4x L2)",
+            "cpu_baseline": oracle_line(t_call, cpu)}
 
 
 def bench_crossover(args, torch, tql):
+    """Both paths at every M on both MLP geometries. Each (M, path) time
+    replays a CUDA graph of calls over distinct weight copies (> 4x L2 in
+    total), so no call finds its trellis in L2. The CPU oracle runs in full
+    for the configured M up to 1024 and on 128 seeded rows above."""
     out = {}
     Ms = (16, 32, 64, 128) if args.quick else tuple(sorted(set((16, 32, 48, 384, 512, 768) + synthetic.PREFILL_MS)))
+    reps = 2 if args.quick else 3
     for gm in synthetic.PREFILL_GEOMS:
         K, N, bits = gm["K"], gm["N"], 4
-        mat = DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED))
+        nc = copies_for(K * N * bits // 8)
+        mats = [DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED, matrix_index=j))
+                for j in range(nc)]
         ws = make_ws(torch, tql, max(Ms), K, N, bits, 1)
         rows = []
         mx = None
         for M in Ms:
             x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
             y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-            it = 3 if M >= 1024 else 8
-            td = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 0, ws, tql.EXL3_F16), it, 1)
-            tp = time_fn(torch, lambda: call_linear(tql, x, M, mat, y, 1, ws, tql.EXL3_F16), it, 1)
-            rows.append({"M": M, "decode_ms": round(td, 4), "prefill_ms": round(tp, 4)})
+            td = graph_time(torch, [lambda m=m: call_linear(tql, x, M, m, y, 0, ws, tql.EXL3_F16) for m in mats], reps)
+            tp = graph_time(torch, [lambda m=m: call_linear(tql, x, M, m, y, 1, ws, tql.EXL3_F16) for m in mats], reps)
+            row = {"M": M, "decode_ms": round(td, 4), "prefill_ms": round(tp, 4)}
+            if M in synthetic.PREFILL_MS and not args.quick:
+                cpu = oracle_call_time(K, N, bits, M, synthetic.PREFILL_SEED, rows=None if M <= 1024 else 128)
+                row["cpu_baseline"] = oracle_line(min(td, tp), cpu)
+            rows.append(row)
             if mx is None and tp < td:
                 mx = M
-        out[gm["name"]] = {"rows": rows, "crossover_M": mx}
-        del ws, mat
+            del x, y
+        out[gm["name"]] = {"rows": rows, "crossover_M": mx,
+                           "timing": f"CUDA graph replays over {nc} weight copies "
+                                     f"({nc * mats[0].nbytes / 1e6:.0f} MB > 4x L2)"}
+        del ws, mats
+        torch.cuda.empty_cache()
     return out
 
 
 def bench_logits(args, torch, tql, peaks):
+    """Odd-vocab masked logits (the weight alone, 953 MB, is > 4x L2).
+    Times replay a CUDA graph of calls."""
     c = synthetic.LOGITS
     K, ns, ng, nd, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
     mat = DevMatrix(torch, synthetic.make_matrix(K, ns, bits, seed=c["seed"]), n_gemm=ng)
@@ -494,14 +588,20 @@ def bench_logits(args, torch, tql, peaks):
         lg = torch.empty((M, ng), dtype=torch.float32, device="cuda")
         am = torch.empty((M,), dtype=torch.int32, device="cuda")
         fn = lambda: tql.exl3_logits_masked(x, M, K, mat.trellis, bits, ns, ng, nd, mat.su, mat.sv, lg, am, 128, ws)
-        t = time_fn(torch, fn, 3 if M >= 2048 else 10, 1)
+        t = graph_time(torch, [fn] * (2 if M >= 2048 else 4), 3 if M >= 2048 else 10)
         r = {"ms": round(t, 4), "path": "prefill" if M >= 128 else "decode"}
         if M >= 128:
             r["tflops"] = round(2.0 * M * K * ng / (t * 1e-3) / 1e12, 1)
         else:
             r["weight_gbs"] = round(wbytes / (t * 1e-3) / 1e9, 1)
             r["frac_hbm"] = round(r["weight_gbs"] / peaks["hbm_gbs"], 4)
+        if not args.quick:
+            # oracle on one reconstruct chunk's columns (and 128 rows at M=2048), scaled to the call
+            cpu = oracle_call_time(K, ns, bits, M, c["seed"], rows=None if M <= 16 else 128, cols=32768)
+            r["cpu_baseline"] = oracle_line(t, cpu)
         res[str(M)] = r
+        del x, lg, am
+    res["timing"] = "CUDA graph replays; the 953 MB weight alone exceeds 4x L2"
     return res
 
 
@@ -575,10 +675,21 @@ def bench_mlp_stack(args, torch, tql):
             split["gemm"] += L * times * (t_call - t_had - t_rec)
             del xr, wt
         flops = 2.0 * M * (2 * d * f + f * d) * L
+        cpu_s, samples = 0.0, []
+        if not args.quick:
+            # oracle: layer 0's three projections on 128 seeded rows, scaled to M rows and L layers
+            for j, (K, N) in enumerate(((d, f), (d, f), (f, d))):
+                c1 = oracle_call_time(K, N, bits, M, st["seed_base"], rows=128, matrix_index=j)
+                cpu_s += c1["s"] * L
+                samples.append(c1["sample"])
         out[f"bits{bits}"] = {"layers": L, "ms_per_pass": round(ms, 3), "tok_per_s": round(M / (ms * 1e-3), 1),
                               "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                               "split_ms": {k: round(v, 3) for k, v in split.items()},
                               "first_nonfinite_layer": first_bad, "clocks": clk,
+                              "cpu_baseline": oracle_line(ms, {"s": cpu_s, "extrapolated": True,
+                                                               "sample": "layer 0 gate, up, down on 128 rows each: "
+                                                                         + "; ".join(samples) + f"; x {L} layers",
+                                                               "cores": c1["cores"]}) if samples else None,
                               "trellis_gb": round(sum(m["tr"].numel() * 2 for lay in layers for m in lay) / 1e9, 2)}
         del layers, ws
         torch.cuda.empty_cache()
@@ -633,7 +744,17 @@ def bench_decode_stack(args, torch, tql, peaks):
             with torch.cuda.graph(gr, stream=stream):
                 one_step()
             graph_ms = time_fn(torch, gr.replay, 20, 3)
-        out[f"M{M}"] = {"eager_ms": round(eager_ms, 3), "graph_ms": round(graph_ms, 3),
+        cpu = None
+        if not args.quick:
+            cpu_s, samples = 0.0, []
+            for j, (K, N) in enumerate(((d, f), (d, f), (f, d))):
+                c1 = oracle_call_time(K, N, bits, M, st["seed_base"], x_scale=0.05, matrix_index=j)
+                cpu_s += c1["s"] * L
+                samples.append(c1["sample"])
+            cpu = oracle_line(graph_ms, {"s": cpu_s, "extrapolated": True, "cores": c1["cores"],
+                                         "sample": "layer 0 gate, up, down in full: " + "; ".join(samples)
+                                                   + f"; x {L} layers"})
+        out[f"M{M}"] = {"eager_ms": round(eager_ms, 3), "graph_ms": round(graph_ms, 3), "cpu_baseline": cpu,
                         "graph_speedup": round(eager_ms / graph_ms, 3),
                         "graph_weight_gbs": round(wbytes / (graph_ms * 1e-3) / 1e9, 1),
                         "graph_frac_hbm": round(wbytes / (graph_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -700,33 +821,54 @@ def profile_call(spec: str):
     torch.cuda.synchronize()
 
 
-def run_reference(args, dist):
+def headline_config(world: int) -> dict:
+    """The workload both arms measure (the GB300 arm and the oracle arm)."""
+    return {"workload": synthetic.GATE_DECODE["name"], "step": "exl3_linear at M=1,4,8,16 (fp16 out)",
+            "parallelism": f"replicas x{world}"}
+
+
+def run_reference(args, dist, budget_s: float = 150.0):
+    """Reference arm: the CPU oracle on the host cores, on the headline step
+    (the four calls at M = 1, 4, 8, 16), exactly --warmup untimed and --steps
+    timed steps. Each step covers output columns [0, cols) of every call,
+    with cols (a multiple of 128, at most N) sized so that the whole run
+    stays within about budget_s seconds."""
     world, rank, _ = dist
     if rank != 0:
         return
     import oracle
-    base = oracle_sample(0.5)
-    cols = base["cols"]
+    oracle.build()
     g = synthetic.GATE_DECODE
-    K, N, bits = g["K"], g["N"], g["bits"]
+    K, N, bits, Ms = g["K"], g["N"], g["bits"], g["Ms"]
     mat = synthetic.make_matrix(K, N, bits, seed=g["seed"])
-    x = synthetic.make_activations(16, K, seed=g["seed"], x_scale=g["x_scale"])
-    steps = max(1, min(args.steps, 20))
-    warm = max(0, min(args.warmup, 3))
-    for _ in range(warm):
-        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+    xs = {M: synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"]) for M in Ms}
+
+    def step(cols):
+        for M in Ms:
+            oracle.linear(xs[M], mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
+
+    t128 = float("inf")
+    for _ in range(2):
+        t0 = time.perf_counter()
+        step(128)
+        t128 = min(t128, time.perf_counter() - t0)
+    n_steps = max(1, args.steps + args.warmup)
+    cols = int(max(1, min(N // 128, budget_s / n_steps / t128))) * 128
+    for _ in range(args.warmup):
+        step(cols)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle.linear(x, mat.trellis, bits, K, N, mat.su, mat.sv, 0, cols)
-    dt = (time.perf_counter() - t0) / steps
-    bytes_ = K * cols * bits // 8
+    for _ in range(args.steps):
+        step(cols)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    bytes_ = len(Ms) * K * cols * bits // 8
     v = bytes_ / dt / 1e9
+    sample = f"each step the four calls (M = 1, 4, 8, 16, full K) over output columns [0, {cols}) of {N}"
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": synthetic.GATE_DECODE["name"], "sample_cols": cols, "rows": 16},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": headline_config(world),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"each step one M=16 call over columns [0, {cols}) (full K)"},
+                             "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -781,11 +923,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
-            "config": {"workload": synthetic.GATE_DECODE["name"], "step": "exl3_linear at M=1,4,8,16 (fp16 out)",
-                       "l2": f"inputs larger than L2: {WEIGHT_COPIES} rotating weight copies "
+            "config": headline_config(world),
+            "timing": {"l2": f"inputs larger than L2: {WEIGHT_COPIES} rotating weight copies "
                              f"({WEIGHT_COPIES * dec['mats'][0].nbytes / 1e6:.0f} MB)",
-                       "timing": "CUDA graph replays, CUDA events on the launching stream",
-                       "parallelism": f"replicas x{world}"},
+                       "method": "CUDA graph replays, CUDA events on the launching stream"},
             "roofline": dec["roofline"], "clocks": dec["clocks"], "e2e": e2e,
             "gpu_launches": dec["gpu_launches"], "per_m": dec["per_m"], "cpu_baseline": cpu,
             "device_status": status,

@@ -274,8 +274,8 @@ exl3_status exl3_silu_mul(const void *gate, const void *up, void *out, int64_t n
 exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
 
 /*
- * exl3_linear_decode_noalloc: the decode-shaped exl3_linear (as with
- * m_threshold == 0) for callers that cannot allocate device memory: a
+ * exl3_linear_decode_noalloc: the decode-shaped linear layer for callers
+ * that cannot allocate device memory: a
  * plugin inside a host program that owns every device buffer, or code that
  * must not call cudaMalloc at run time because it synchronises the whole
  * device. The caller passes only inputs and outputs; the split-K partial
@@ -283,11 +283,20 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
  * library (a static device array that every GPU which loads libexl3.so
  * keeps until the process exits). The pages have no counterpart to this
  * entry point.
- *   Arguments as exl3_linear, without m_threshold and workspace.
+ *   Arguments as exl3_linear, without m_threshold and workspace; the same
+ *   shape, row-count, bit-width and alignment rules, with the same status
+ *   codes.
+ *   Kernels: the rows run in groups of up to 16 through the 16-row
+ *   decode-shaped kernel (exactly what exl3_linear runs for M <= 16). For
+ *   M > 16 exl3_linear switches to its tensor-core kernel, which needs a
+ *   rotated copy of all M rows in the workspace; this entry point instead
+ *   repeats the 16-row kernel ceil(M/16) times, so its cost grows about
+ *   ceil(M/16)-fold over the M = 16 call (results agree with exl3_linear
+ *   within the layer tolerance, not bit for bit).
  *   Limit: exl3_linear_workspace_bytes(16, K, n_gemm, bits, 0) must not
- *   exceed 24 MiB (the MLP projections fit; a 248192-wide logits layer does
- *   not); larger problems return EXL3_ERR_NOALLOC_TOO_LARGE and launch
- *   nothing.
+ *   exceed EXL3_NOALLOC_SCRATCH_BYTES (24 MiB; the MLP projections fit, a
+ *   248192-wide logits layer does not); larger problems return
+ *   EXL3_ERR_NOALLOC_TOO_LARGE and launch nothing.
  *   The first call on a device looks up the buffer's device address, so
  *   make that first call before any stream capture. No call needs the
  *   buffer to start at zero. Every call shares the one buffer
@@ -295,6 +304,7 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
  *   GPU (different streams, no ordering) race: order them. It never calls
  *   cudaMalloc, cudaFree or any allocating routine. exl3_init must have run.
  */
+#define EXL3_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
 exl3_status exl3_linear_decode_noalloc(const void *x, int64_t M, int64_t K, const uint16_t *trellis,
                                        int bits, int64_t n_stored, int64_t n_gemm, const void *su,
                                        const void *sv, void *y, int y_dtype, void *stream);

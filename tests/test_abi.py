@@ -115,11 +115,14 @@ def test_decode_plan_gate_geometry_fills_every_sm(lib):
     assert ctas == 152 and slots == 15
 
 
-def test_noalloc_limit_covers_mlp_geometries(lib):
-    lim = 24 << 20
+@pytest.mark.parametrize("sms", [132, 148, 152, 160])
+def test_noalloc_limit_covers_mlp_geometries(lib, sms):
+    lim = tql.EXL3_NOALLOC_SCRATCH_BYTES
+    with open(os.path.join(ROOT, "include", "exl3.h")) as f:
+        assert "#define EXL3_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)" in f.read()
     for K, N, bits in ((5120, 17408, 4), (17408, 5120, 4), (5120, 17408, 3)):
-        assert tql.exl3_linear_workspace_bytes_for(16, K, N, bits, 0, 152) <= lim
-    assert tql.exl3_linear_workspace_bytes_for(16, 5120, 248192, 6, 0, 152) > lim
+        assert tql.exl3_linear_workspace_bytes_for(16, K, N, bits, 0, sms) <= lim
+    assert tql.exl3_linear_workspace_bytes_for(16, 5120, 248192, 6, 0, sms) > lim
 
 
 def test_weight_rotated_workspace_is_one_slice(lib):
@@ -171,6 +174,16 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert L.exl3_hadamard128(good, good + 8, None, 2, 128, None) == 2
     # self-test limit out of range
     assert L.exl3_selftest_wait_timeout(0, None) == 1
+    # the no-alloc entry point applies the same shape, row and bit rules
+    assert L.exl3_linear_decode_noalloc(good, 4, 100, good, 4, 256, 256, good, good, good, 1, None) == 1
+    assert L.exl3_linear_decode_noalloc(good, 4, 128, good, 4, big, 256, good, good, good, 1, None) == 1
+    assert L.exl3_linear_decode_noalloc(good, 4, 128, good, 4, 256, 384, good, good, good, 1, None) == 1
+    assert L.exl3_linear_decode_noalloc(good, -1, 128, good, 4, 256, 256, good, good, good, 1, None) == 1
+    assert L.exl3_linear_decode_noalloc(good, (1 << 31) + 1, 128, good, 4, 256, 256, good, good, good, 1,
+                                        None) == 1
+    assert L.exl3_linear_decode_noalloc(good, 4, 128, good, 4, 256, 256, good, good, good, 5, None) == 1
+    assert L.exl3_linear_decode_noalloc(good, 4, 128, good, 9, 256, 256, good, good, good, 1, None) == 3
+    assert L.exl3_linear_decode_noalloc(good + 4, 4, 128, good, 4, 256, 256, good, good, good, 1, None) == 2
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

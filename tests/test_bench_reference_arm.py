@@ -10,7 +10,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_reference_arm_prints_one_contract_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3", "--warmup", "2"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -21,9 +21,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference"
     assert d["metric"] == bench.METRIC
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
-    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
+    # the driver's step and warm-up counts are honoured exactly
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 2
     assert d["ms_per_step"] > 0
-    assert d["data"] == "synthetic" and "workload" in d["config"]
+    assert d["data"] == "synthetic" and d["config"] == bench.headline_config(1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     e = d["e2e"]

@@ -81,7 +81,8 @@ def test_reconstruct_bit_exact(oracle, bits, layout, n0, n_cols):
     assert np.array_equal(got, ref)
 
 
-def test_reconstruct_full_gate_geometry_sampled(oracle):
+def test_reconstruct_full_gate_geometry(oracle):
+    """The whole 5120 x 17408 gate_proj weight, both layouts, bit for bit."""
     torch = torch_mod()
     K, N, bits = 5120, 17408, 4
     m = synthetic.make_matrix(K, N, bits, seed=1)
@@ -92,9 +93,8 @@ def test_reconstruct_full_gate_geometry_sampled(oracle):
     tql.exl3_reconstruct(tr, bits, K, N, 0, N, wt, tql.EXL3_LAYOUT_NK)
     torch.cuda.synchronize()
     assert torch.equal(w.t().contiguous(), wt)
-    for c0 in (0, 8704, N - 128):
-        ref = oracle.reconstruct(m.trellis, bits, K, N, c0, 128).view(np.uint16)
-        assert np.array_equal(w[:, c0:c0 + 128].cpu().numpy().view(np.uint16), ref)
+    ref = oracle.reconstruct(m.trellis, bits, K, N).view(np.uint16)
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), ref)
 
 
 # ---------------------------------------------------------------------------
@@ -133,14 +133,17 @@ def test_linear_fused_decode_path(oracle, K, N, bits, M):
 
 
 @pytest.mark.parametrize("M", [24, 64, 256])
-def test_fused_decode_full_gate_geometry_sampled(oracle, M):
+def test_fused_decode_full_gate_geometry(oracle, M):
+    """The tensor-core decode-shaped kernel on the whole gate_proj geometry
+    (K=5120, N=17408): every output column against the oracle. Its stream-K
+    plan puts a different k-step boundary in every n-block, so no block is
+    left unchecked."""
     K, N, bits = 5120, 17408, 4
     m = synthetic.make_matrix(K, N, bits, seed=2)
     x = synthetic.make_activations(M, K, seed=2)
     y = Layer(m).linear(to_dev(x), DECODE).cpu().numpy()
-    for b in (0, 77, N // 128 - 1):
-        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
-        assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, b
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
 
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (256, 256, 1), (384, 256, 7)])
@@ -265,69 +268,111 @@ def test_logits_mask_and_argmax_small(oracle, thr, M):
 # full-size workloads, checked on sampled 128-column blocks
 # ---------------------------------------------------------------------------
 
-def test_decode_gate_full_size_sampled(oracle):
+def test_decode_gate_full_size(oracle):
+    """The decode-shaped headline workload (gate_proj K=5120 N=17408 bits=4,
+    M = 1, 4, 8, 16): every output column of every call against the oracle.
+    The stream-K decode splits each of the 136 n-blocks at a different k
+    slab, so every n-block exercises its own slot boundary."""
     g = synthetic.GATE_DECODE
     K, N, bits = g["K"], g["N"], g["bits"]
     m = synthetic.make_matrix(K, N, bits, seed=g["seed"])
     L = Layer(m)
-    blocks = (0, 67, N // 128 - 1)
     for M in g["Ms"]:
         x = synthetic.make_activations(M, K, seed=g["seed"], x_scale=g["x_scale"])
         y = L.linear(to_dev(x), DECODE).cpu().numpy()
-        for b in blocks:
-            ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
-            assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, (M, b)
+        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+        assert rel_err(y, ref) <= TOL, M
 
 
 @pytest.mark.parametrize("geom", [0, 1])
-def test_prefill_full_size_sampled(oracle, geom):
+def test_prefill_full_size_sampled_rows(oracle, geom):
+    """Prefill-shaped calls at full size (gate 5120->17408 at M=2048, down
+    17408->5120 at M=1024): 128 evenly spaced rows, every output column."""
     gm = synthetic.PREFILL_GEOMS[geom]
     K, N, bits = gm["K"], gm["N"], 4
     M = 2048 if geom == 0 else 1024
     m = synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED)
     x = synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED)
-    L = Layer(m)
-    y = L.linear(to_dev(x), 128).cpu().numpy()
-    for b in (0, N // 128 - 1):
-        ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv, 128 * b, 128)
-        assert rel_err(y[:, 128 * b:128 * b + 128], ref) <= TOL, b
+    y = Layer(m).linear(to_dev(x), 128)
+    rows = np.arange(0, M, M // 128)
+    got = y[rows].cpu().numpy()
+    ref = oracle.linear(x[rows], m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(got, ref) <= TOL
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 2048])
-def test_logits_full_size(oracle, M):
+@pytest.mark.parametrize("M,thr,n_rows", [(1, 128, 1), (16, 128, 16), (64, 128, 16), (2048, 128, 64)])
+def test_logits_full_vocab(oracle, M, thr, n_rows):
+    """Odd-vocab logits (K=5120, n_stored=248320, n_gemm=248192,
+    n_decodable=248077, bits=6) at M = 1, 16 (the 16-row decode kernel), 64
+    (the tensor-core decode kernel) and 2048 (prefill-shaped): the pad is
+    -inf, the rest finite, the GPU argmax equals the CPU argmax of the GPU's
+    own buffer on every row, and on n_rows evenly spaced rows every logit
+    and the greedy pick are checked against the oracle over the whole vocab."""
     c = synthetic.LOGITS
     K, n_stored, n_gemm, n_dec, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
     assert tql.exl3_aligned_logits_width(n_dec, n_stored) == n_gemm
     m = synthetic.make_matrix(K, n_stored, bits, seed=c["seed"])
     x = synthetic.make_activations(M, K, seed=c["seed"])
     L = Layer(m, n_gemm=n_gemm)
-    lg, am = L.logits(to_dev(x), n_dec, 128)
+    lg, am = L.logits(to_dev(x), n_dec, thr)
     torch = torch_mod()
     assert bool(torch.isneginf(lg[:, n_dec:]).all())
     assert bool(torch.isfinite(lg[:, :n_dec]).all())
     assert torch.equal(am.long(), torch.argmax(lg, dim=1))
-    rows = slice(0, min(M, 64))
-    xs = x[rows]
-    for b in (0, n_gemm // 128 - 1):
-        ref = oracle.linear(xs, m.trellis, bits, K, n_stored, m.su, m.sv, 128 * b, 128)
-        got = lg[rows, 128 * b:128 * b + 128].cpu().numpy()
-        fin = np.arange(128 * b, 128 * b + 128) < n_dec
-        assert rel_err(got[:, fin], ref[:, fin]) <= TOL
-
-
-def test_logits_full_size_argmax_against_oracle(oracle):
-    c = synthetic.LOGITS
-    K, n_stored, n_gemm, n_dec, bits = c["K"], c["n_stored"], c["n_gemm"], c["n_decodable"], c["bits"]
-    m = synthetic.make_matrix(K, n_stored, bits, seed=c["seed"])
-    x = synthetic.make_activations(2, K, seed=c["seed"])
-    L = Layer(m, n_gemm=n_gemm)
-    lg, am = L.logits(to_dev(x), n_dec, 0)
-    ref, ref_am = oracle.logits_masked(x, m.trellis, bits, K, n_stored, n_gemm, n_dec, m.su, m.sv)
+    rows = np.arange(0, M, M // n_rows)
+    ref, ref_am = oracle.logits_masked(x[rows], m.trellis, bits, K, n_stored, n_gemm, n_dec, m.su, m.sv)
+    got = lg[torch.from_numpy(rows).cuda()].cpu().numpy()
     fin = np.isfinite(ref)
-    lgn = lg.cpu().numpy()
-    assert rel_err(lgn[fin], ref[fin]) <= TOL
+    assert np.array_equal(fin, np.isfinite(got))
+    assert rel_err(got[fin], ref[fin]) <= TOL
     rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
-    argmax_agrees(am.cpu().numpy(), ref, 2 * TOL * rms)
+    argmax_agrees(am.cpu().numpy()[rows], ref, 2 * TOL * rms)
+
+
+# Each kernel path that writes logits applies the pad mask itself. A case per
+# path: the pad covers columns that path writes, and the decodable width is
+# chosen below row 0's unmasked maximum, so a path that dropped the mask would
+# leave a finite pad column and let the pad win row 0's argmax. The planted
+# mistake lives in the oracle (skip_mask): with it, row 0's pick lands in the
+# pad, which is what the checks below would then catch.
+MASK_PATHS = {
+    # 16-row stream-K decode kernel, n-blocks shared by several warps (slot reduction)
+    "decode_slot_reduction": dict(K=256, n_stored=640, n_gemm=512, bits=6, M=6, thr=0),
+    # the same kernel on a wide, shallow layer: warps that own whole n-blocks finish them in place
+    "decode_whole_block": dict(K=128, n_stored=248320, n_gemm=248192, bits=6, M=3, thr=0),
+    # tensor-core decode kernel (16 < M), its slot reduction
+    "fused_decode": dict(K=256, n_stored=640, n_gemm=512, bits=6, M=40, thr=0),
+    # prefill GEMM: whole-tile epilogue over two reconstruct chunks
+    "prefill_epilogue": dict(K=256, n_stored=33408, n_gemm=33152, bits=4, M=256, thr=1),
+    # prefill GEMM: last partial wave split along K, reduced by its finalize kernel
+    "prefill_split_tail": dict(K=2048, n_stored=512, n_gemm=384, bits=4, M=6, thr=1),
+}
+
+
+@pytest.mark.parametrize("path", sorted(MASK_PATHS))
+def test_pad_mask_on_every_logits_path(oracle, path):
+    c = MASK_PATHS[path]
+    K, ns, ng, bits, M, thr = c["K"], c["n_stored"], c["n_gemm"], c["bits"], c["M"], c["thr"]
+    m = synthetic.make_matrix(K, ns, bits, seed=K + ns + M)
+    x = synthetic.make_activations(M, K, seed=M + 7)
+    raw = oracle.linear(x, m.trellis, bits, K, ns, m.su, m.sv, 0, ng)
+    # pad starts below row 0's unmasked maximum (and within the first 300 columns,
+    # so that it spans every n-block, tile and chunk after it)
+    n_dec = max(1, min(int(np.argmax(raw[0])), 300))
+    ref, ref_am = oracle.logits_masked(x, m.trellis, bits, K, ns, ng, n_dec, m.su, m.sv)
+    _, bad_am = oracle.logits_masked(x, m.trellis, bits, K, ns, ng, n_dec, m.su, m.sv, skip_mask=True)
+    assert bad_am[0] >= n_dec  # the planted mistake is visible to these checks
+    lg, am = Layer(m, n_gemm=ng).logits(to_dev(x), n_dec, thr)
+    lg = lg.cpu().numpy()
+    am = am.cpu().numpy()
+    assert np.all(np.isneginf(lg[:, n_dec:]))
+    assert np.all(np.isfinite(lg[:, :n_dec]))
+    assert np.all(am < n_dec)
+    assert np.array_equal(am, np.argmax(lg, axis=1))
+    fin = np.isfinite(ref)
+    assert rel_err(lg[fin], ref[fin]) <= TOL
+    rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
+    argmax_agrees(am, ref, 2 * TOL * rms)
 
 
 def test_silu_mul_glue():

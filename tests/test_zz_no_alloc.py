@@ -5,8 +5,9 @@ that owns every device buffer, or code that must not call cudaMalloc at run
 time because it synchronises the whole device. exl3_linear_decode_noalloc
 serves them with the library's own fixed 24 MiB scratch buffer. These tests
 call it through the C ABI twice in a row and compare each result with the
-ordinary exl3_linear (decode-shaped, caller-provided workspace) within the
-tolerance the parity tests use. This file is collected last on purpose.
+ordinary exl3_linear (decode-shaped, caller-provided workspace) and with the
+CPU oracle, within the tolerance the parity tests use. This file is
+collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -40,7 +41,7 @@ def _noalloc(L, xd, y_dtype):
 
 
 @pytest.mark.parametrize("K,N,bits,Ms", [(5120, 17408, 4, (1, 16)), (512, 512, 4, (37, 5)), (640, 384, 6, (9, 2))])
-def test_noalloc_matches_linear_on_two_calls(K, N, bits, Ms):
+def test_noalloc_matches_linear_on_two_calls(oracle, K, N, bits, Ms):
     m = synthetic.make_matrix(K, N, bits, seed=K + N)
     L = Layer(m)
     for call, M in enumerate(Ms):  # two calls in a row, different inputs
@@ -49,6 +50,8 @@ def test_noalloc_matches_linear_on_two_calls(K, N, bits, Ms):
         ref = L.linear(xd, 0, tql.EXL3_F32).cpu().numpy().astype(np.float64)
         got = _noalloc(L, xd, tql.EXL3_F32).cpu().numpy()
         assert rel_err(got, ref) <= TOL, (M, call)
+        # and against the oracle directly (M = 37 runs row groups of 16, 16 and 5)
+        assert rel_err(got, oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)) <= TOL, (M, call)
         got16 = _noalloc(L, xd, tql.EXL3_F16).cpu().numpy()
         assert np.array_equal(got16.view(np.uint16), got.astype(np.float16).view(np.uint16))
     assert tql.exl3_get_device_status() == 0
@@ -56,9 +59,13 @@ def test_noalloc_matches_linear_on_two_calls(K, N, bits, Ms):
 
 def test_noalloc_rejects_problems_beyond_its_buffer():
     torch = torch_mod()
+    lim = tql.EXL3_NOALLOC_SCRATCH_BYTES
+    # on this device's SM count: the MLP projections fit the buffer, the logits layer does not
+    for K, N, bits in ((5120, 17408, 4), (17408, 5120, 4), (5120, 17408, 3)):
+        assert tql.exl3_linear_workspace_bytes(16, K, N, bits, 0) <= lim
     c = synthetic.LOGITS
     K, ns, ng = c["K"], c["n_stored"], c["n_gemm"]
-    assert tql.exl3_linear_workspace_bytes(16, K, ng, c["bits"], 0) > 24 << 20
+    assert tql.exl3_linear_workspace_bytes(16, K, ng, c["bits"], 0) > lim
     x = torch.zeros((1, K), dtype=torch.float16, device="cuda")
     tr = torch.zeros((16,), dtype=torch.int16, device="cuda")
     su = torch.zeros((K,), dtype=torch.float16, device="cuda")

@@ -14,7 +14,7 @@ import threading
 
 __all__ = [
     "Exl3Error", "build", "load", "EXL3_F16", "EXL3_F32", "EXL3_LAYOUT_KN", "EXL3_LAYOUT_NK",
-    "EXL3_RECONSTRUCT_CHUNK_COLS", "exl3_init", "exl3_status_string", "exl3_supported_bits",
+    "EXL3_RECONSTRUCT_CHUNK_COLS", "EXL3_NOALLOC_SCRATCH_BYTES", "exl3_init", "exl3_status_string", "exl3_supported_bits",
     "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_linear_workspace_bytes_for",
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
@@ -30,6 +30,7 @@ EXL3_F32 = 1
 EXL3_LAYOUT_KN = 0
 EXL3_LAYOUT_NK = 1
 EXL3_RECONSTRUCT_CHUNK_COLS = 32768
+EXL3_NOALLOC_SCRATCH_BYTES = 24 << 20
 
 STATUS_NAMES = {
     0: "EXL3_OK", 1: "EXL3_ERR_INVALID_ARG", 2: "EXL3_ERR_ALIGNMENT", 3: "EXL3_ERR_UNSUPPORTED_BITS",
@@ -243,7 +244,8 @@ def exl3_selftest_wait_timeout(limit_us: int, stream=None) -> None:
 def exl3_linear_decode_noalloc(x, M: int, K: int, trellis, bits: int, n_stored: int, n_gemm: int, su, sv, y,
                                y_dtype: int, stream=None) -> None:
     """Decode-shaped linear layer that allocates nothing: its scratch is a
-    fixed 16 MiB buffer inside the library (see include/exl3.h)."""
+    fixed buffer of EXL3_NOALLOC_SCRATCH_BYTES (24 MiB) inside the library.
+    Rows run in groups of 16 through the 16-row decode kernel."""
     _check(load().exl3_linear_decode_noalloc(_ptr(x), int(M), int(K), _ptr(trellis), int(bits), int(n_stored),
                                              int(n_gemm), _ptr(su), _ptr(sv), _ptr(y), int(y_dtype),
                                              _stream(stream)), "exl3_linear_decode_noalloc")

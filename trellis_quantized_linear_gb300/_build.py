@@ -19,7 +19,6 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libexl3.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
-EXTRA: list[str] = []  # extra nvcc flags (compile-time tuning knobs)
 
 
 def _nvcc() -> str:
@@ -51,7 +50,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     common = [nvcc, "-std=c++17", ARCH, "-O3", "-lineinfo", "-Xcompiler", "-fPIC",
-              "-I", os.path.join(ROOT, "include")] + list(EXTRA)
+              "-I", os.path.join(ROOT, "include")]
     if verbose:
         common += ["-Xptxas", "-v"]
 

@@ -31,11 +31,6 @@ const DeviceInfo *current_device() {
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool shape_ok(int64_t K, int64_t n_stored, int64_t n_gemm) {
-  return K > 0 && K % 128 == 0 && K <= 131072 && n_gemm > 0 && n_gemm % 128 == 0 && n_stored % 128 == 0 &&
-         n_gemm <= n_stored && n_stored <= ((int64_t)1 << 24);
-}
-
 exl3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA; }
 
 // Shared by exl3_linear and exl3_logits_masked once arguments are validated.
@@ -136,7 +131,7 @@ exl3_status validate_linear(const void *x, int64_t M, int64_t K, const uint16_t 
                             int64_t n_stored, int64_t n_gemm, const void *su, const void *sv, const void *y,
                             int64_t m_threshold, void *workspace, size_t workspace_bytes,
                             const DeviceInfo **dev_out, WorkspaceLayout *layout) {
-  if (M < 0 || M > (int64_t)1 << 31 || m_threshold < 0 || !shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
+  if (!linear_rows_ok(M) || m_threshold < 0 || !linear_shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
   if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
   if (!aligned16(x) || !aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(y) ||
       !aligned16(workspace))
@@ -239,7 +234,7 @@ const char *exl3_status_string(int status) {
     case EXL3_ERR_NOT_INITIALIZED: return "exl3_init was not called for the current device";
     case EXL3_ERR_CUDA: return "CUDA runtime error or failed launch";
     case EXL3_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
-    case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed 24 MiB no-alloc buffer";
+    case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed no-alloc buffer holds";
     default: return "unknown status";
   }
 }
@@ -333,7 +328,7 @@ exl3_status exl3_linear_weight_rotated(const void *x, int64_t M, int64_t K, cons
                                        int64_t n_stored, int64_t n_gemm, const void *su, const void *sv, void *y,
                                        int y_dtype, void *workspace, size_t workspace_bytes, void *stream) {
   if (y_dtype != EXL3_F16 && y_dtype != EXL3_F32) return EXL3_ERR_INVALID_ARG;
-  if (M < 0 || M > (int64_t)1 << 31 || !shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
+  if (!linear_rows_ok(M) || !linear_shape_ok(K, n_stored, n_gemm)) return EXL3_ERR_INVALID_ARG;
   if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
   if (!aligned16(x) || !aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(y) ||
       !aligned16(workspace))

@@ -8,11 +8,19 @@
 
 namespace exl3 {
 
-constexpr int kDecodeConsumerWarps = 8;   // consumer warps per decode-GEMM CTA
-constexpr int kDecodeMaxKSplit = 2048;    // largest K range one decode CTA rotates into smem
 constexpr int kDecodeRows = 16;           // activation rows per decode-GEMM launch
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shape rules every linear-layer entry point enforces before any launch:
+// K and n_gemm multiples of 128, n_stored a multiple of 128 and at most 2^24
+// columns, n_gemm <= n_stored, K <= 131072.
+inline bool linear_shape_ok(int64_t K, int64_t n_stored, int64_t n_gemm) {
+  return K > 0 && K % 128 == 0 && K <= 131072 && n_gemm > 0 && n_gemm % 128 == 0 && n_stored % 128 == 0 &&
+         n_gemm <= n_stored && n_stored <= ((int64_t)1 << 24);
+}
+// Activation rows every linear-layer entry point accepts: 0 .. 2^31.
+inline bool linear_rows_ok(int64_t M) { return M >= 0 && M <= ((int64_t)1 << 31); }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Stream-K assignment of the decode-shaped GEMM, per token-group variant

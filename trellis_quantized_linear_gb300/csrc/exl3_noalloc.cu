@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = size_t(24) << 20;  // 24 MiB
+constexpr size_t kNoallocScratchBytes = EXL3_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -45,8 +45,7 @@ extern "C" exl3_status exl3_linear_decode_noalloc(const void *x, int64_t M, int6
                                                   int bits, int64_t n_stored, int64_t n_gemm, const void *su,
                                                   const void *sv, void *y, int y_dtype, void *stream) {
   using namespace exl3;
-  if (M < 0 || K <= 0 || K % 128 || K > 131072 || n_gemm <= 0 || n_gemm % 128 || n_stored % 128 ||
-      n_gemm > n_stored || (y_dtype != EXL3_F16 && y_dtype != EXL3_F32))
+  if (!linear_rows_ok(M) || !linear_shape_ok(K, n_stored, n_gemm) || (y_dtype != EXL3_F16 && y_dtype != EXL3_F32))
     return EXL3_ERR_INVALID_ARG;
   if (!bits_supported(bits)) return EXL3_ERR_UNSUPPORTED_BITS;
   if (!aligned16(x) || !aligned16(trellis) || !aligned16(su) || !aligned16(sv) || !aligned16(y))
