@@ -8,28 +8,29 @@
 //
 // Up to three kernels per launch:
 //   1. rotate_frag_kernel: x' = RNE_fp16(had_r_128(x * su)) for the (<= 16)
-//      rows, written in mma fragment order (per 16-row k slab, lane (g, q)
-//      finds x'[g][4q..4q+3] and x'[g+8][4q..4q+3] as 8 or 16 contiguous
-//      bytes).
+//      rows, written in mma fragment order: per 16-row k slab, lane (g, q)
+//      finds its B registers as 16 contiguous bytes (for <= 8 rows already
+//      in the {x', 0} form the duplicated-weight mma takes).
 //   2. decode_gemm_kernel: stream-K over all (n-block, k-slab) work. A slab
 //      is 16 k-rows x 128 output columns = 8 horizontally adjacent trellis
-//      tiles, 256*BITS contiguous bytes. The P = SMs x warps-per-CTA warps
-//      each own a contiguous range of slabs in n-block-major order, so every
-//      warp on every SM has the same amount of work. Each warp feeds itself:
-//      lane 0 streams its slabs (weights plus the slab's x' fragments) into a
-//      private ring in shared memory with cp.async.bulk, one mbarrier per
-//      stage.
+//      tiles, 256*BITS contiguous bytes. The P = SMs x 12 warps each own a
+//      contiguous range of slabs in n-block-major order, so every warp on
+//      every SM has the same amount of work. Each warp feeds itself: lane 0
+//      streams chunks of up to 4 slabs (one 2-D TMA copy of the trellis plus
+//      one bulk copy of the chunk's x' fragments) into a private ring of
+//      stages in shared memory, one mbarrier per stage.
 //      Lane (g, q) decodes tile g, rows 4q..4q+3 straight into m16n8k16 A
 //      fragments (A = W^T: mma row r <-> output column 16*(r%8) + j +
-//      8*(r/8) for mma j), B = x'^T (8 tokens per mma). Each A register
-//      holds one weight in both halves and the matching B register {x', 0}:
-//      mma k index 2q <-> tile row 4q and 2q+8 <-> row 4q+1 in the first
-//      mma of a column group, rows 4q+2 and 4q+3 in the second (odd k
-//      indices multiply zeros). This spends twice the mmas (tensor pipe
-//      ~20 % busy) to save the two instructions per weight pair that would
-//      pack two decoded weights into one register. After 16 mmas per slab
-//      and token group, lane (g, q) holds output columns 16g .. 16g+15 of
-//      tokens 2q, 2q+1 (+8).
+//      8*(r/8) for mma j), B = x'^T (8 tokens per mma). For <= 8 rows each A
+//      register holds one weight in both halves and the matching B register
+//      {x', 0}: mma k index 2q <-> tile row 4q and 2q+8 <-> row 4q+1 in the
+//      first mma of a column group, rows 4q+2 and 4q+3 in the second (odd k
+//      indices multiply zeros). This spends twice the mmas (the tensor pipe
+//      has room) to save the instructions that would pack two decoded
+//      weights into one register. For 9..16 rows the registers hold weight
+//      pairs (rows 4q and 4q+1, rows 4q+2 and 4q+3) and one mma per column
+//      group and token group. After a slab, lane (g, q) holds output columns
+//      16g .. 16g+15 of tokens 2q, 2q+1 (+8).
 //      When a warp finishes its part of an n-block it either owns the whole
 //      n-block (then it applies had_r_128 over the 128 columns, sv and the
 //      -inf mask and writes y), or it stores an fp32 partial in its slot.
@@ -38,118 +39,45 @@
 //      applies had_r_128, sv and the mask and writes y.
 //
 // Roofline: HBM-bound on the trellis bytes (K*N*BITS/8 per launch) unless
-// the per-weight integer decode (a half-rate ALU pipe) binds first.
+// the per-weight integer decode (a half-rate ALU pipe) binds first, which
+// it does on GB300: per weight one window extraction, one IMAD (LCG), one
+// LOP3 (mask and xor) and one fp16 add, plus an mma per 4 weights.
 #include <cuda.h>
 #include <math.h>
 
 #include "exl3_common.cuh"
 #include "exl3_internal.h"
 
-// Tuning knobs (compile-time): warps per CTA for <= 8 rows.
-#ifndef EXL3_DECODE_WARPS_M8
-#define EXL3_DECODE_WARPS_M8 12
-#endif
-// ... and for 9..16 rows.
-#ifndef EXL3_DECODE_WARPS_M16
-#define EXL3_DECODE_WARPS_M16 12
-#endif
-// Packing of two decoded fp16 weights into one mma register, per variant
-// (0: byte permute on the integer pipe; 1: multiply-add on the fp16 pipe).
-#ifndef EXL3_DECODE_PACK_FMA_M8
-#define EXL3_DECODE_PACK_FMA_M8 1
-#endif
-#ifndef EXL3_DECODE_PACK_FMA_M16
-#define EXL3_DECODE_PACK_FMA_M16 1
-#endif
-// A operand form, per variant (1: each weight duplicated in both halves of
-// its register against zero-interleaved x', two mmas per slab and column
-// group; 0: two weights packed per register, one mma).
-#ifndef EXL3_DECODE_DUP_M8
-#define EXL3_DECODE_DUP_M8 1
-#endif
-#ifndef EXL3_DECODE_DUP_M16
-#define EXL3_DECODE_DUP_M16 0
-#endif
-// Where the end of this warp's part of an n-block is tested, per variant
-// (1: once per chunk, after its last slab; 0: after every slab).
-#ifndef EXL3_DECODE_BLOCK_PER_CHUNK_M8
-#define EXL3_DECODE_BLOCK_PER_CHUNK_M8 1
-#endif
-#ifndef EXL3_DECODE_BLOCK_PER_CHUNK_M16
-#define EXL3_DECODE_BLOCK_PER_CHUNK_M16 0
-#endif
-// Nibble-shifted window copy made on the FMA pipe for BITS = 4 (see
-// Windows; 1: on). Also taking the offset-0 and offset-4 states from the
-// high word of a multiply (IMAD.HI) measured 18 % slower at 1 row.
-#ifndef EXL3_DECODE_FMA_EXTRACT_M8
-#define EXL3_DECODE_FMA_EXTRACT_M8 1
-#endif
-#ifndef EXL3_DECODE_FMA_EXTRACT_M16
-#define EXL3_DECODE_FMA_EXTRACT_M16 0
-#endif
-// Slabs per inner-loop iteration, per variant (for <= 8 rows two measured
-// 1-1.5 % faster than one and 3 % faster than four; for 9..16 rows two
-// spills and is 2 % slower than one).
-#ifndef EXL3_DECODE_UNROLL_M8
-#define EXL3_DECODE_UNROLL_M8 2
-#endif
-#ifndef EXL3_DECODE_UNROLL_M16
-#define EXL3_DECODE_UNROLL_M16 1
-#endif
-#ifndef EXL3_DECODE_STAGES_M8
-#define EXL3_DECODE_STAGES_M8 2
-#endif
-// Proxy fence after reading a ring stage (1) or none (0): the stage's words
-// are consumed by register-dependent decode work before the warp reaches the
-// reissue point, so the reuse is ordered without it.
-#ifndef EXL3_DECODE_PROXY_FENCE
-#define EXL3_DECODE_PROXY_FENCE 0
-#endif
-// Programmatic dependent launch between the rotation, decode and finalize
-// kernels (1: on).
-#ifndef EXL3_DECODE_PDL
-#define EXL3_DECODE_PDL 1
-#endif
-// Most rows for which the slot reduction runs one warp per CTA.
-#ifndef EXL3_DECODE_FIN_1W_ROWS
-#define EXL3_DECODE_FIN_1W_ROWS 2
-#endif
-// The input rotation, too, as a programmatic dependent of whatever precedes
-// it in the stream (1: on).
-#ifndef EXL3_DECODE_ROTATE_PDL
-#define EXL3_DECODE_ROTATE_PDL 1
-#endif
-
 namespace exl3 {
 
 namespace {
 
-#ifndef EXL3_DECODE_CHUNK
-#define EXL3_DECODE_CHUNK 4  // slabs per copy for BITS <= 4 (half that above)
-#endif
+// Warps per CTA (one CTA per SM) for <= 8 rows and for 9..16 rows.
+template <int MT>
+constexpr int dec_warps() { return MT == 1 ? 12 : 12; }
+constexpr int kXFrag = 512;     // x' fragment bytes per 16-row k slab (32 lanes x 16 B)
 
 template <int BITS, int MT>
 struct DecodeCfg {
-  static constexpr int kWarps = MT == 1 ? EXL3_DECODE_WARPS_M8 : EXL3_DECODE_WARPS_M16;  // warps per CTA
+  static constexpr int kWarps = dec_warps<MT>();
   static constexpr int kSeg = 256 * BITS;                    // trellis bytes per slab
-  static constexpr int kChunk = BITS <= 4 ? EXL3_DECODE_CHUNK : (EXL3_DECODE_CHUNK + 1) / 2;  // slabs per copy
-  static constexpr int kStages = MT == 1 ? EXL3_DECODE_STAGES_M8 : 3;  // ring stages (chunks) per warp
-  static constexpr int kXB = 32 * 4 * MT * 2;                // x' fragment bytes per slab
-  static constexpr int kStage = kChunk * kSeg;
+  static constexpr int kChunk = BITS <= 4 ? 4 : 2;           // slabs per copy
+  static constexpr int kStages = MT == 1 ? 2 : 3;            // ring stages (chunks) per warp
+  static constexpr int kStage = kChunk * (kSeg + kXFrag);    // trellis box, then the chunk's x'
   static constexpr int kWarpRing = kStages * kStage;
   static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8;
+  static_assert(kSmem <= 227 * 1024, "decode ring exceeds shared memory");
 };
 
 struct DecodeParams {
-  const uint8_t *trellis;
-  const uint8_t *xf;  // rotated x in fragment order, K/16 slabs of 256*MT bytes
+  const uint8_t *xf;  // rotated x in fragment order, K/16 slabs of kXFrag bytes
   const __half *sv;
   void *y;
   float *partials;
   int *status;
-  int64_t tiles_n, n_gemm, n_valid, TS, P;
-  int rows, y_f32, KT, smax;
-  uint32_t m16;  // 16, opaque to the compiler (see Windows)
+  int64_t n_gemm, n_valid;
+  int TS, P, KT, rows, y_f32, smax;
+  uint32_t m16;  // 16, opaque to the compiler (a multiply by it stays on the FMA pipe)
 };
 
 __device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
@@ -316,44 +244,95 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 // dependency) start its prologue now.
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// The 16 window states of one tile row for BITS = 4. A and B hold the row's
+// own words w0..w3 as two little-endian uint32 (w1 << 16 | w0, w3 << 16 | w2);
+// P holds the stream word just before the row in its high half. State c is
+// the 16-bit window ending at row bit 4c + 3, earliest bit most significant.
+// Per row: two byte permutes and two multiplies build the views that
+// straddle a register boundary (p|w0, w1|w2, and their 4-bit shifts); the
+// 4-bit shifts of w0|w1 and w2|w3 are rotations of A and B; then every state
+// is one instruction.
+__device__ __forceinline__ void row4_states(uint32_t A, uint32_t B, uint32_t P, uint32_t m16, uint32_t (&s)[16]) {
+  const uint32_t xc0 = __byte_perm(A, P, 0x7610);  // p << 16 | w0
+  const uint32_t xc1 = __byte_perm(B, A, 0x7610);  // w1 << 16 | w2
+  const uint32_t y0 = xc0 * m16, y1 = xc1 * m16;   // the same, 4 bits further (low nibble unused)
+  const uint32_t ya = __funnelshift_l(A, A, 20);   // (w0 << 16 | w1) << 4 (low nibble unused)
+  const uint32_t yb = __funnelshift_l(B, B, 20);   // (w2 << 16 | w3) << 4
+  s[0] = y0 >> 16;
+  s[1] = __byte_perm(xc0, 0u, 0x4421);
+  s[2] = __byte_perm(y0, 0u, 0x4421);
+  s[3] = A & 0xFFFFu;
+  s[4] = ya >> 16;
+  s[5] = __byte_perm(A, 0u, 0x4403);
+  s[6] = __byte_perm(ya, 0u, 0x4421);
+  s[7] = A >> 16;
+  s[8] = y1 >> 16;
+  s[9] = __byte_perm(xc1, 0u, 0x4421);
+  s[10] = __byte_perm(y1, 0u, 0x4421);
+  s[11] = B & 0xFFFFu;
+  s[12] = yb >> 16;
+  s[13] = __byte_perm(B, 0u, 0x4403);
+  s[14] = __byte_perm(yb, 0u, 0x4421);
+  s[15] = B >> 16;
+}
+
+// The lane's 64 states of one slab: st[r][c] = tile row 4q + r, column c.
+template <int BITS>
+__device__ __forceinline__ void slab_states(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16,
+                                            uint32_t (&st)[4][16]) {
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) row4_states(own[2 * r], own[2 * r + 1], r == 0 ? prev : own[2 * r - 1], m16, st[r]);
+  } else {
+    RowWindows<BITS> rw;
+    rw.build(own, prev);
+    static_for<4>([&](auto R) {
+      static_for<16>([&](auto C) { st[R.value][C.value] = rw.template state<R.value, C.value>(); });
+    });
+  }
+}
+
 template <int BITS, int MT>
 __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using Cfg = DecodeCfg<BITS, MT>;
-  constexpr int R = Cfg::kStages;
+  constexpr int R = Cfg::kStages, CHK = Cfg::kChunk;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int64_t pw = (int64_t)blockIdx.x * Cfg::kWarps + warp;
+  const int pw = blockIdx.x * Cfg::kWarps + warp;
   if (pw >= p.P) return;
-  const int64_t z0 = pw * p.TS / p.P, z1 = (pw + 1) * p.TS / p.P;
-
+  const int z0 = (int)((int64_t)pw * p.TS / p.P), z1 = (int)((int64_t)(pw + 1) * p.TS / p.P);
+  const int KT = p.KT;
   uint8_t *ring = smem + warp * Cfg::kWarpRing;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kWarps * Cfg::kWarpRing) + warp * R;
   const uint32_t ring_s = smem_u32(ring);
+  const uint32_t bar0 = smem_u32(smem + Cfg::kWarps * Cfg::kWarpRing) + warp * R * 8;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < R; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_barrier_init();
   }
   __syncwarp();
 
-  // Issue cursor (lane 0 only): the next chunk to stream in. A chunk is up
-  // to kChunk consecutive k slabs of one n-block, fetched by one 2-D TMA copy
-  // (box: one slab row of 8 tiles x kChunk tile rows; rows past K read as 0).
-  constexpr int CHK = Cfg::kChunk;
-  const int KT = p.KT;
-  int i_nb = (int)(z0 / KT), i_tk = (int)(z0 % KT), i_st = 0;
-  int64_t zi = z0;
-  int64_t issued = 0;
-  auto issue_next = [&]() {
-    const int64_t left = z1 - zi;
-    const int len = (int)((KT - i_tk) < CHK ? ((int64_t)(KT - i_tk) < left ? (KT - i_tk) : left)
-                                            : (CHK < left ? CHK : left));
-    const uint32_t bar = smem_u32(&bars[i_st]);
-    mbar_arrive_expect_tx(bar, Cfg::kStage);
+  // Producer cursor (lane 0 only): the next chunk to stream in. A chunk is
+  // up to CHK consecutive k slabs of one n-block: one 2-D TMA copy of the
+  // trellis (box: one slab row of 8 tiles x CHK tile rows; rows past K read
+  // as zero and are never used) and one bulk copy of the chunk's x'.
+  int i_nb = z0 / KT, i_tk = z0 - i_nb * KT, i_z = z0, i_st = 0, issued = 0;
+  auto chunk_len = [&](int tk, int z) { return min(min(CHK, KT - tk), z1 - z); };
+  auto issue_trellis = [&]() {
+    const int len = chunk_len(i_tk, i_z);
+    const uint32_t bar = bar0 + 8 * i_st;
+    mbar_arrive_expect_tx(bar, CHK * Cfg::kSeg + len * kXFrag);
     tma_load_2d_u64(ring_s + i_st * Cfg::kStage, &tmap, bar, i_nb * (32 * BITS), i_tk);
-    zi += len;
+    return len;
+  };
+  auto issue_x = [&](int st, int tk, int len) {
+    bulk_g2s(ring_s + st * Cfg::kStage + CHK * Cfg::kSeg, p.xf + (size_t)tk * kXFrag, len * kXFrag,
+             bar0 + 8 * st);
+  };
+  auto advance = [&](int len) {
+    i_z += len;
     i_tk += len;
     if (i_tk == KT) {
       i_tk = 0;
@@ -362,11 +341,27 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     if (++i_st == R) i_st = 0;
     ++issued;
   };
+  // Fill the ring with trellis before waiting for the rotation kernel (the
+  // weights do not depend on it); the x' halves follow after the wait.
+  int pro_tk[R], pro_len[R];
   if (lane == 0) {
-    for (int c = 0; c < R - 1 && zi < z1; ++c) issue_next();
+#pragma unroll
+    for (int c = 0; c < R; ++c) {
+      pro_len[c] = 0;
+      if (i_z < z1) {
+        pro_tk[c] = i_tk;
+        pro_len[c] = issue_trellis();
+        advance(pro_len[c]);
+      }
+    }
   }
   allow_next_grid();
   wait_prior_grid();  // x' comes from the rotation kernel
+  if (lane == 0) {
+#pragma unroll
+    for (int c = 0; c < R; ++c)
+      if (pro_len[c]) issue_x(c, pro_tk[c], pro_len[c]);
+  }
 
   float acc[MT][8][4];
 #pragma unroll
@@ -374,31 +369,12 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
 
-  // Consumer cursor.
-  int nb = (int)(z0 / KT), tk = (int)(z0 % KT), s = 0;
-  uint32_t phase = 0;
-  int64_t consumed = 0;
-  // x' fragments of the current slab, loaded one slab ahead.
-  uint32_t bx[2 * MT], bx_next[2 * MT];
-  auto load_x = [&](int k_slab, uint32_t (&dst)[2 * MT]) {
-    if constexpr (MT == 1) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p.xf + (int64_t)k_slab * Cfg::kXB) + lane);
-      dst[0] = v.x;
-      dst[1] = v.y;
-    } else {
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xf + (int64_t)k_slab * Cfg::kXB) + lane);
-      dst[0] = v.x;
-      dst[1] = v.y;
-      dst[2] = v.z;
-      dst[3] = v.w;
-    }
-  };
   // This warp's part of n-block cnb is complete: finish it or store the
   // partial, then clear the accumulators.
-  auto block_end = [&](const int64_t cnb) {
-    float v[MT][2][16];
-    const bool whole = (z0 <= cnb * p.KT) && (z1 >= (cnb + 1) * p.KT);
+  auto block_end = [&](const int cnb) {
+    const bool whole = (z0 <= cnb * KT) && (z1 >= (cnb + 1) * KT);
     if (whole) {
+      float v[MT][2][16];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -410,11 +386,11 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
           }
       finish_block<MT>(v, p, cnb, lane);
     } else {
-      // Store this warp's contribution in its slot; decode_finalize_kernel
-      // sums the n-block's slots in slot order.
-      const int64_t pf = slab_owner(cnb * p.KT, p.P, p.TS);
+      // this warp's contribution goes to its slot; decode_finalize_kernel
+      // sums the n-block's slots in slot order
+      const int64_t pf = slab_owner((int64_t)cnb * KT, p.P, p.TS);
       const int64_t slot_elems = (int64_t)8 * MT * 128;
-      float *part = p.partials + (cnb * p.smax + (pw - pf)) * slot_elems;
+      float *part = p.partials + ((int64_t)cnb * p.smax + (pw - pf)) * slot_elems;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -434,19 +410,52 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
   };
-  constexpr bool kPerChunk = MT == 1 ? EXL3_DECODE_BLOCK_PER_CHUNK_M8 : EXL3_DECODE_BLOCK_PER_CHUNK_M16;
-  int xk = tk;  // k slab of bx_next
-  load_x(xk, bx_next);
-  int64_t z = z0;
+
+  // One slab: the lane's 64 weights (tile g, rows 4q..4q+3) into 16 (or,
+  // for 9..16 rows, 2 x 8) mmas. tr: the slab's trellis in the stage; xb:
+  // the lane's 16 bytes of x' fragments for the slab.
+  auto slab = [&](const uint8_t *tr, const uint8_t *xb) {
+    uint32_t own[2 * BITS];
+    load_own_words<BITS, true>(tr + lane * 8 * BITS, own);
+    const uint4 bxv = *reinterpret_cast<const uint4 *>(xb + lane * 16);
+    const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
+    uint32_t st[4][16];
+    slab_states<BITS>(own, prev, p.m16, st);
+    if constexpr (MT == 1) {
+      // B registers {x'[row], 0} for tile rows 4q .. 4q+3 of token g
+      static_for<8>([&](auto J) {
+        constexpr int j = J.value;
+        mma16816(acc[0][j], decode_dup(st[0][j]), decode_dup(st[0][j + 8]), decode_dup(st[1][j]),
+                 decode_dup(st[1][j + 8]), bxv.x, bxv.y);
+        mma16816(acc[0][j], decode_dup(st[2][j]), decode_dup(st[2][j + 8]), decode_dup(st[3][j]),
+                 decode_dup(st[3][j + 8]), bxv.z, bxv.w);
+      });
+    } else {
+      // B registers: {x'[4q], x'[4q+1]}, {x'[4q+2], x'[4q+3]} of tokens g and g + 8
+      static_for<8>([&](auto J) {
+        constexpr int j = J.value;
+        const uint32_t a0 = decode_pair_sel<true>(st[0][j], st[1][j]);
+        const uint32_t a1 = decode_pair_sel<true>(st[0][j + 8], st[1][j + 8]);
+        const uint32_t a2 = decode_pair_sel<true>(st[2][j], st[3][j]);
+        const uint32_t a3 = decode_pair_sel<true>(st[2][j + 8], st[3][j + 8]);
+        mma16816(acc[0][j], a0, a1, a2, a3, bxv.x, bxv.y);
+        mma16816(acc[1][j], a0, a1, a2, a3, bxv.z, bxv.w);
+      });
+    }
+  };
+
+  // Consumer cursor.
+  int nb = z0 / KT, tk = z0 - nb * KT, z = z0, s = 0, consumed = 0;
+  uint32_t phase = 0;
   while (z < z1) {
-    if (lane == 0 && zi < z1) issue_next();
+    const int len = chunk_len(tk, z);
     // warp-uniform outcome: a lane that gave up takes the whole warp out
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[s]), phase, p.status))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * s, phase, p.status))) {
       if (lane == 0) {  // let this warp's copies in flight land before it retires
         int ws = s;
         uint32_t wp = phase;
-        for (int64_t u = consumed; u < issued; ++u) {
-          mbar_wait_short(smem_u32(&bars[ws]), wp);
+        for (int u = consumed; u < issued; ++u) {
+          mbar_wait_short(bar0 + 8 * ws, wp);
           if (++ws == R) {
             ws = 0;
             wp ^= 1u;
@@ -456,101 +465,35 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
       return;
     }
     const uint8_t *stage = ring + s * Cfg::kStage;
-    const int64_t left = z1 - z;
-    const int len = (int)((KT - tk) < CHK ? ((int64_t)(KT - tk) < left ? (KT - tk) : left)
-                                          : (CHK < left ? CHK : left));
-    // A chunk lies inside one n-block, so only its last slab can end this
-    // warp's part of an n-block (kPerChunk tests it once per chunk).
-    constexpr int kUnroll = MT == 1 ? EXL3_DECODE_UNROLL_M8 : EXL3_DECODE_UNROLL_M16;
-#pragma unroll(kUnroll)
-    for (int i = 0; i < len; ++i) {
-      uint32_t own[2 * BITS];
-      load_own_words<BITS, true>(stage + i * Cfg::kSeg + lane * 8 * BITS, own);
-#pragma unroll
-      for (int r = 0; r < 2 * MT; ++r) bx[r] = bx_next[r];
-      // x' of the next k slab (none past the end of this warp's range)
-      if constexpr (kPerChunk) {
-        xk = xk + 1 == KT ? 0 : xk + 1;
-      } else {
-        xk = tk + 1 == KT ? 0 : tk + 1;  // tk: this slab
-      }
-      if (z + i + 1 < z1) load_x(xk, bx_next);
-      const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-      constexpr bool kFx = MT == 1 ? EXL3_DECODE_FMA_EXTRACT_M8 : EXL3_DECODE_FMA_EXTRACT_M16;
-      Windows<BITS, kFx> win;
-      win.build(own, prev, p.m16);
-      constexpr bool kDup = MT == 1 ? EXL3_DECODE_DUP_M8 : EXL3_DECODE_DUP_M16;
-      if constexpr (kDup) {
-        // B registers {x'[k], 0} for slab rows 4q .. 4q+3 of each token group.
-        uint32_t bz[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          bz[mt][0] = bx[2 * mt] & 0xFFFFu;
-          bz[mt][1] = bx[2 * mt] >> 16;
-          bz[mt][2] = bx[2 * mt + 1] & 0xFFFFu;
-          bz[mt][3] = bx[2 * mt + 1] >> 16;
-        }
-        static_for<8>([&](auto J) {
-          constexpr int j = J.value;
-          // rows 4q, 4q+1 of the lane's tile (mma k 2q and 2q+8), then 4q+2, 4q+3
-          const uint32_t a0 = decode_dup(win.template state<0, j>());
-          const uint32_t a1 = decode_dup(win.template state<0, j + 8>());
-          const uint32_t a2 = decode_dup(win.template state<1, j>());
-          const uint32_t a3 = decode_dup(win.template state<1, j + 8>());
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bz[mt][0], bz[mt][1]);
-          const uint32_t c0 = decode_dup(win.template state<2, j>());
-          const uint32_t c1 = decode_dup(win.template state<2, j + 8>());
-          const uint32_t c2 = decode_dup(win.template state<3, j>());
-          const uint32_t c3 = decode_dup(win.template state<3, j + 8>());
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], c0, c1, c2, c3, bz[mt][2], bz[mt][3]);
-        });
-      } else {
-        static_for<8>([&](auto J) {
-          constexpr int j = J.value;
-          constexpr bool kPF = MT == 1 ? EXL3_DECODE_PACK_FMA_M8 : EXL3_DECODE_PACK_FMA_M16;
-          const uint32_t a0 = decode_pair_sel<kPF>(win.template state<0, j>(), win.template state<1, j>());
-          const uint32_t a1 = decode_pair_sel<kPF>(win.template state<0, j + 8>(), win.template state<1, j + 8>());
-          const uint32_t a2 = decode_pair_sel<kPF>(win.template state<2, j>(), win.template state<3, j>());
-          const uint32_t a3 = decode_pair_sel<kPF>(win.template state<2, j + 8>(), win.template state<3, j + 8>());
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][j], a0, a1, a2, a3, bx[2 * mt], bx[2 * mt + 1]);
-        });
-      }
-      if constexpr (!kPerChunk) {
-        const bool done = (tk == KT - 1) || (z + i == z1 - 1);
-        const int cur_nb = nb;
-        if (++tk == KT) {
-          tk = 0;
-          ++nb;
-        }
-        if (done) block_end(cur_nb);
-      }
-    }  // slabs of this chunk
-    if constexpr (kPerChunk) {
-      tk += len;
-      if (tk == KT || z + len == z1) {
-        block_end(nb);
-        if (tk == KT) {
-          tk = 0;
-          ++nb;
-        }
+    const uint8_t *xst = stage + CHK * Cfg::kSeg;
+#pragma unroll 2
+    for (int i = 0; i < len; ++i) slab(stage + i * Cfg::kSeg, xst + i * kXFrag);
+    // a chunk lies inside one n-block, so only its end can end this warp's part of it
+    tk += len;
+    z += len;
+    if (tk == KT || z == z1) {
+      block_end(nb);
+      if (tk == KT) {
+        tk = 0;
+        ++nb;
       }
     }
-    __syncwarp();  // every lane has consumed this stage before lane 0 refills it
-#if EXL3_DECODE_PROXY_FENCE
-    fence_proxy_async_shared();
-#endif
+    // every lane has read this stage (its words are in registers and consumed
+    // by register-dependent work) before lane 0 hands it to the next copy
+    __syncwarp();
+    if (lane == 0 && i_z < z1) {
+      const int itk = i_tk, ist = i_st;
+      const int ilen = issue_trellis();
+      issue_x(ist, itk, ilen);
+      advance(ilen);
+    }
     if (++s == R) {
       s = 0;
       phase ^= 1u;
     }
-    z += len;
     ++consumed;
   }
 }
-
 
 // Sums the partial slots of every n-block shared by several warps, in slot
 // order, then applies had_r_128 over the block's 128 columns, sv and the
@@ -564,7 +507,7 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
                                                               int rows, int64_t P, int64_t TS, int KT, int all_blocks) {
   // The next op's input rotation may launch now; it waits for this grid
   // before it touches memory.
-  if (EXL3_DECODE_ROTATE_PDL) allow_next_grid();
+  allow_next_grid();
   const int lane = threadIdx.x & 31;
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nb = w / rows;
@@ -592,7 +535,7 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
                                                              int rows, int64_t P, int64_t TS, int KT) {
   constexpr int SC = 4;
   const int lane = threadIdx.x & 31;
-  if (EXL3_DECODE_ROTATE_PDL) allow_next_grid();  // as in decode_finalize_kernel
+  allow_next_grid();  // as in decode_finalize_kernel
   const unsigned groups = (unsigned)((rows + RPW - 1) / RPW);
   const unsigned w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nb = w / groups;
@@ -633,14 +576,15 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
 }
 
 // x' = RNE_fp16(had_r_128(x * su)) for up to 8*MT rows, in fragment order:
-// for k slab tk, lane (g, q) owns 4*MT halves at xf[(tk*32 + 4g + q)*4*MT],
-// {x'[g][16tk+4q .. +3], x'[g+8][16tk+4q .. +3]}. Rows >= `rows` are zero.
+// for k slab tk, lane (g, q) owns the 16 bytes at xf + (tk*32 + 4g + q)*16.
+// MT = 1 (up to 8 rows): the B registers of the duplicated-weight mma,
+// {x'[g][16tk+4q+i], 0} for i = 0..3. MT = 2: {x'[g][16tk+4q .. +3],
+// x'[g+8][16tk+4q .. +3]}. Rows >= `rows` are zero.
 // One half-warp per (row, 128-block): lane l16 holds elements 8*l16 .. +7,
 // butterfly stages h = 1, 2, 4 in-lane and 8 .. 64 across lanes.
 template <int MT>
 __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restrict__ x, const __half *__restrict__ su,
-                                                          int rows, int64_t K, __half *__restrict__ xf) {
-  constexpr int CH = 4 * MT;
+                                                          int rows, int64_t K, uint8_t *__restrict__ xf) {
   allow_next_grid();
   // When launched as a programmatic dependent of the previous kernel in the
   // stream (only its launch latency is hidden): x may be that kernel's
@@ -686,19 +630,22 @@ __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restri
         v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
       }
     if (valid) {
-      __half2 hv[4];
+      uint32_t hb[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(v[2 * e] * kInvSqrt128, v[2 * e + 1] * kInvSqrt128);
+      for (int i = 0; i < 8; ++i) hb[i] = __half_as_ushort(__float2half_rn(v[i] * kInvSqrt128));
+      // elements 8*l16 .. +7 of block kb: slab kb*8 + l16/2, tile rows
+      // 8*(l16&1) .. +7, i.e. lanes q = 2*(l16&1) and q + 1 of group m & 7
       const int64_t tk = kb * 8 + (l16 >> 1);
       const int qq = 2 * (l16 & 1);
-      const int gg = m & 7;
-      const int off = (m >> 3) * 4;
-      __half *d0 = xf + (tk * 32 + gg * 4 + qq) * CH + off;
-      __half *d1 = xf + (tk * 32 + gg * 4 + qq + 1) * CH + off;
-      *reinterpret_cast<uint2 *>(d0) =
-          make_uint2(*reinterpret_cast<uint32_t *>(&hv[0]), *reinterpret_cast<uint32_t *>(&hv[1]));
-      *reinterpret_cast<uint2 *>(d1) =
-          make_uint2(*reinterpret_cast<uint32_t *>(&hv[2]), *reinterpret_cast<uint32_t *>(&hv[3]));
+      uint8_t *d0 = xf + (tk * 32 + (m & 7) * 4 + qq) * 16;
+      if constexpr (MT == 1) {
+        *reinterpret_cast<uint4 *>(d0) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+        *reinterpret_cast<uint4 *>(d0 + 16) = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+      } else {
+        const int off = (m >> 3) * 8;
+        *reinterpret_cast<uint2 *>(d0 + off) = make_uint2(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16);
+        *reinterpret_cast<uint2 *>(d0 + 16 + off) = make_uint2(hb[4] | hb[5] << 16, hb[6] | hb[7] << 16);
+      }
     }
   }
 }
@@ -725,10 +672,10 @@ cudaError_t init_bits() {
   return init_one<BITS, 2>();
 }
 
-// Launches `kernel` after the previous work in `st`; with EXL3_DECODE_PDL its
-// prologue may overlap the tail of the previous kernel (programmatic
-// dependency), and the kernel itself waits before reading that kernel's
-// output.
+// Launches `kernel` after the previous work in `st` as a programmatic
+// dependent: its prologue may overlap the tail of the previous kernel, and
+// the kernel itself waits (griddepcontrol.wait) before reading that
+// kernel's output.
 template <typename... Params, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, unsigned block, size_t smem, cudaStream_t st,
                              Args... args) {
@@ -741,17 +688,18 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, unsigned bloc
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = EXL3_DECODE_PDL ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int BITS, int MT>
-cudaError_t launch_bits(const DecodeParams &dp, int64_t grid, cudaStream_t st) {
+cudaError_t launch_bits(const DecodeParams &dp, const uint16_t *trellis, int64_t tiles_n, int64_t grid,
+                        cudaStream_t st) {
   // The trellis as rows of 16-row tile strips (8-byte elements): one row is
   // every tile of one k slab; the box is one n-block's slab x kChunk rows.
   alignas(64) CUtensorMap tmap;
-  const uint64_t row_elems = (uint64_t)dp.tiles_n * 4 * BITS;
-  if (!encode_tensor_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, dp.trellis, row_elems, (uint64_t)dp.KT,
+  const uint64_t row_elems = (uint64_t)tiles_n * 4 * BITS;
+  if (!encode_tensor_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, trellis, row_elems, (uint64_t)dp.KT,
                             row_elems * 8, 32 * BITS, DecodeCfg<BITS, MT>::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   return launch_dependent(decode_gemm_kernel<BITS, MT>, (unsigned)grid, DecodeCfg<BITS, MT>::kWarps * 32,
@@ -759,16 +707,17 @@ cudaError_t launch_bits(const DecodeParams &dp, int64_t grid, cudaStream_t st) {
 }
 
 template <int MT>
-cudaError_t launch_mt(int bits, const DecodeParams &dp, int64_t grid, cudaStream_t st) {
+cudaError_t launch_mt(int bits, const DecodeParams &dp, const uint16_t *trellis, int64_t tiles_n, int64_t grid,
+                      cudaStream_t st) {
   switch (bits) {
-    case 1: return launch_bits<1, MT>(dp, grid, st);
-    case 7: return launch_bits<7, MT>(dp, grid, st);
-    case 2: return launch_bits<2, MT>(dp, grid, st);
-    case 3: return launch_bits<3, MT>(dp, grid, st);
-    case 4: return launch_bits<4, MT>(dp, grid, st);
-    case 5: return launch_bits<5, MT>(dp, grid, st);
-    case 6: return launch_bits<6, MT>(dp, grid, st);
-    case 8: return launch_bits<8, MT>(dp, grid, st);
+    case 1: return launch_bits<1, MT>(dp, trellis, tiles_n, grid, st);
+    case 2: return launch_bits<2, MT>(dp, trellis, tiles_n, grid, st);
+    case 3: return launch_bits<3, MT>(dp, trellis, tiles_n, grid, st);
+    case 4: return launch_bits<4, MT>(dp, trellis, tiles_n, grid, st);
+    case 5: return launch_bits<5, MT>(dp, trellis, tiles_n, grid, st);
+    case 6: return launch_bits<6, MT>(dp, trellis, tiles_n, grid, st);
+    case 7: return launch_bits<7, MT>(dp, trellis, tiles_n, grid, st);
+    case 8: return launch_bits<8, MT>(dp, trellis, tiles_n, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -782,7 +731,7 @@ DecodePlan decode_plan(int64_t n_blocks, int64_t k_blocks, int num_sms) {
   const int64_t KT = k_blocks * 8;
   const int64_t TS = n_blocks * KT;
   for (int mt = 1; mt <= 2; ++mt) {
-    const int warps = mt == 1 ? DecodeCfg<4, 1>::kWarps : DecodeCfg<4, 2>::kWarps;
+    const int warps = mt == 1 ? dec_warps<1>() : dec_warps<2>();
     int64_t P = (int64_t)num_sms * warps;
     if (P > TS) P = TS;
     int64_t smax = 1;
@@ -806,12 +755,12 @@ size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks) {
 cudaError_t init_decode_kernels() {
   cudaError_t e;
   if ((e = init_bits<1>()) != cudaSuccess) return e;
-  if ((e = init_bits<7>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
   if ((e = init_bits<4>()) != cudaSuccess) return e;
   if ((e = init_bits<5>()) != cudaSuccess) return e;
   if ((e = init_bits<6>()) != cudaSuccess) return e;
+  if ((e = init_bits<7>()) != cudaSuccess) return e;
   return init_bits<8>();
 }
 
@@ -820,12 +769,12 @@ cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t 
                                    int units_per_block, int all_blocks, cudaStream_t st) {
   if (!all_blocks) {
     const int64_t warps = (n_gemm / 128) * rows;
-    // One warp per CTA for few rows spreads the slot loads over more SMs
+    // One warp per CTA for 1-2 rows spreads the slot loads over more SMs
     // (0.35 us less at 1 row, 0.1 us at 2; 4 rows measured 0.1 us slower).
-    const unsigned wpc = rows <= EXL3_DECODE_FIN_1W_ROWS ? 1u : 8u;
-    return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, (int64_t)wpc), 32u * wpc, (size_t)0, st, partials,
-                            smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid, rows, P, TS,
-                            units_per_block, all_blocks);
+    const unsigned wpc = rows <= 2 ? 1u : 8u;
+    return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, (int64_t)wpc), 32u * wpc, (size_t)0, st,
+                            partials, smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid,
+                            rows, P, TS, units_per_block, all_blocks);
   }
   const int rpw = rows <= 64 ? 1 : 2;  // measured: 4 rows per warp was 4 % slower at 256 rows
   const unsigned grid = (unsigned)ceil_div((n_gemm / 128) * ceil_div(rows, rpw), 8);
@@ -840,39 +789,38 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   // 1. rotated activations in fragment order
   {
     const int64_t jobs = 8 * MT * (K / 128);
-    int64_t grid = ceil_div(ceil_div(jobs, 2), 8);
+    const unsigned grid = (unsigned)ceil_div(ceil_div(jobs, 2), 8);
     const __half *x = static_cast<const __half *>(L.x), *su = static_cast<const __half *>(L.su);
-    __half *xf = static_cast<__half *>(L.xf);
+    uint8_t *xf = static_cast<uint8_t *>(L.xf);
     cudaError_t e;
-    if (EXL3_DECODE_ROTATE_PDL && MT == 1)  // (measured 0.5 us slower for 9..16 rows)
-      e = launch_dependent(rotate_frag_kernel<1>, (unsigned)grid, 256, 0, st, x, su, L.rows, K, xf);
-    else if (MT == 1)
-      rotate_frag_kernel<1><<<(unsigned)grid, 256, 0, st>>>(x, su, L.rows, K, xf);
-    else
-      rotate_frag_kernel<2><<<(unsigned)grid, 256, 0, st>>>(x, su, L.rows, K, xf);
-    if (!(EXL3_DECODE_ROTATE_PDL && MT == 1)) e = cudaGetLastError();
+    if (MT == 1)  // (a programmatic dependent measured 0.5 us slower for 9..16 rows)
+      e = launch_dependent(rotate_frag_kernel<1>, grid, 256, 0, st, x, su, L.rows, K, xf);
+    else {
+      rotate_frag_kernel<2><<<grid, 256, 0, st>>>(x, su, L.rows, K, xf);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   // 2. stream-K decode GEMM
   DecodeParams dp;
-  dp.trellis = reinterpret_cast<const uint8_t *>(L.trellis);
   dp.xf = static_cast<const uint8_t *>(L.xf);
   dp.sv = static_cast<const __half *>(L.sv);
   dp.y = L.y;
   dp.partials = L.partials;
   dp.status = L.status;
-  dp.tiles_n = L.n_stored / 16;
   dp.n_gemm = L.n_gemm;
   dp.n_valid = L.n_valid;
   dp.KT = (int)(K / 16);
-  dp.TS = (L.n_gemm / 128) * dp.KT;
-  dp.P = L.plan.P[MT - 1];
+  dp.TS = (int)((L.n_gemm / 128) * dp.KT);
+  dp.P = (int)L.plan.P[MT - 1];
   dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
   dp.m16 = 16u;
   dp.y_f32 = L.y_f32;
   const int64_t grid = L.plan.grid[MT - 1];
-  cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, grid, st) : launch_mt<2>(L.bits, dp, grid, st);
+  const int64_t tiles_n = L.n_stored / 16;
+  cudaError_t e = MT == 1 ? launch_mt<1>(L.bits, dp, L.trellis, tiles_n, grid, st)
+                          : launch_mt<2>(L.bits, dp, L.trellis, tiles_n, grid, st);
   if (e != cudaSuccess || dp.smax == 1) return e;
   // 3. reduce the slots of n-blocks shared by several warps
   return launch_decode_finalize(L.partials, dp.smax, (int64_t)8 * MT * 128, L.sv, L.y, L.y_f32, L.n_gemm, L.n_valid,
