@@ -142,29 +142,17 @@ __device__ __forceinline__ uint32_t decode_dup(uint32_t state) {
 }
 
 // Window states of a lane's four rows; for BITS = 4 a nibble-shifted copy
-// of the words makes every state one instruction.
-//
-// kFma (BITS = 4 only) builds the nibble-shifted copy as x * 16 on the FMA
-// pipe instead of a funnel shift on the half-rate integer ALU pipe (only
-// bits 4..31 of a shifted word are ever read, so the low nibble needs no
-// bits from the next word). The multiplier m16 = 16 must come from memory
-// the compiler cannot see (a kernel parameter), or it turns it back into a
-// shift.
-template <int BITS, bool kFma = false>
+// of the words (a funnel shift per word) makes every state one instruction.
+template <int BITS>
 struct Windows {
   RowWindows<BITS> rw;
   uint32_t X4[4 * BITS];
-  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16 = 16u) {
+  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
     rw.build(own, prev);
     if constexpr (BITS == 4) {
-      if constexpr (kFma) {
 #pragma unroll
-        for (int j = 0; j < 4 * BITS; ++j) X4[j] = rw.X[j] * m16;
-      } else {
-#pragma unroll
-        for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
-        X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
-      }
+      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
+      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
     }
   }
   template <int R, int C>

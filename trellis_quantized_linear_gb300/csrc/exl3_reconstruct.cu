@@ -18,25 +18,7 @@
 #include "exl3_common.cuh"
 #include "exl3_internal.h"
 
-// Window form (0: generic shifts; 1: nibble copy by funnel shift for
-// BITS = 4; 2: nibble copy by multiply) and pair packing (0: byte permute
-// on the integer pipe; 1: fp16 multiply-add), compile-time knobs.
-#ifndef EXL3_RECON_WINDOWS
-#define EXL3_RECON_WINDOWS 0
-#endif
-#ifndef EXL3_RECON_PACK_FMA
-#define EXL3_RECON_PACK_FMA 1
-#endif
-
 namespace exl3 {
-
-// State of weight C of row R from the windows (generic shifts with
-// EXL3_RECON_WINDOWS = 0).
-template <int R, int C, typename W>
-__device__ __forceinline__ uint32_t state_of(const W &w) {
-  if constexpr (EXL3_RECON_WINDOWS == 0) return w.rw.template state<R, C>();
-  else return w.template state<R, C>();
-}
 
 // LAYOUT 0 (KN): w[k][j], ld = n_cols.  LAYOUT 1 (NK): w[j][k], ld = K.
 // With `overlap` set the kernel was launched as a programmatic dependent of
@@ -47,7 +29,7 @@ template <int BITS, int LAYOUT>
 __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restrict__ trellis,
                                                           int64_t tiles_n, int64_t tk_count,
                                                           int64_t nb0, int64_t nbc, __half *w,
-                                                          int64_t K, int64_t n_cols, int overlap, uint32_t m16) {
+                                                          int64_t K, int64_t n_cols, int overlap) {
   constexpr int kTileBytes = 32 * BITS;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
@@ -67,19 +49,16 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restr
     uint32_t own[2 * BITS];
     load_own_words<BITS, false>(src, own);
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-    Windows<BITS, EXL3_RECON_WINDOWS == 2 ? 1 : 0> rw;
-    rw.build(own, prev, m16);  // m16 = 16 from a kernel parameter, opaque to the compiler
-    auto pair = [&](uint32_t sa, uint32_t sb) {
-      if constexpr (EXL3_RECON_WINDOWS == 0 && !EXL3_RECON_PACK_FMA) return decode_pair(sa, sb);
-      else return decode_pair_sel<EXL3_RECON_PACK_FMA != 0>(sa, sb);
-    };
+    RowWindows<BITS> rw;
+    rw.build(own, prev);
+    auto pair = [&](uint32_t sa, uint32_t sb) { return decode_pair_sel<true>(sa, sb); };
     const int64_t k0 = tk * 16 + 4 * q;      // first of this lane's 4 rows
     const int64_t j0 = nb * 128 + 16 * g;    // first column of this lane's tile (slice-local)
     if (LAYOUT == 0) {
       static_for<4>([&](auto R) {
         uint32_t p[8];
         static_for<8>([&](auto C2) {
-          p[C2.value] = pair(state_of<R.value, 2 * C2.value>(rw), state_of<R.value, 2 * C2.value + 1>(rw));
+          p[C2.value] = pair(rw.template state<R.value, 2 * C2.value>(), rw.template state<R.value, 2 * C2.value + 1>());
         });
         uint4 *dst = reinterpret_cast<uint4 *>(w + (k0 + R.value) * n_cols + j0);
         dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
@@ -87,8 +66,8 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restr
       });
     } else {
       static_for<16>([&](auto C) {
-        uint32_t lo = pair(state_of<0, C.value>(rw), state_of<1, C.value>(rw));
-        uint32_t hi = pair(state_of<2, C.value>(rw), state_of<3, C.value>(rw));
+        uint32_t lo = pair(rw.template state<0, C.value>(), rw.template state<1, C.value>());
+        uint32_t hi = pair(rw.template state<2, C.value>(), rw.template state<3, C.value>());
         *reinterpret_cast<uint2 *>(w + (j0 + C.value) * K + k0) = make_uint2(lo, hi);
       });
     }
@@ -129,7 +108,7 @@ static cudaError_t launch_one(const uint8_t *t, int64_t tiles_n, int64_t tkc, in
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, reconstruct_kernel<BITS, LAYOUT>, t, tiles_n, tkc, nb0, nbc, w, K, n_cols,
-                            overlap, 16u);
+                            overlap);
 }
 
 template <int BITS>
