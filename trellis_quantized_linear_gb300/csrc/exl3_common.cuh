@@ -178,6 +178,38 @@ struct Windows {
   }
 };
 
+// The 16 window states of one tile row for BITS = 4. A and B hold the row's
+// own words w0..w3 as two little-endian uint32 (w1 << 16 | w0, w3 << 16 | w2);
+// P holds the stream word just before the row in its high half. State c is
+// the 16-bit window ending at row bit 4c + 3, earliest bit most significant.
+// Per row: two byte permutes and two multiplies build the views that
+// straddle a register boundary (p|w0, w1|w2, and their 4-bit shifts); the
+// 4-bit shifts of w0|w1 and w2|w3 are rotations of A and B; then every state
+// is one instruction.
+__device__ __forceinline__ void row4_states(uint32_t A, uint32_t B, uint32_t P, uint32_t m16, uint32_t (&s)[16]) {
+  const uint32_t xc0 = __byte_perm(A, P, 0x7610);  // p << 16 | w0
+  const uint32_t xc1 = __byte_perm(B, A, 0x7610);  // w1 << 16 | w2
+  const uint32_t y0 = xc0 * m16, y1 = xc1 * m16;   // the same, 4 bits further (low nibble unused)
+  const uint32_t ya = __funnelshift_l(A, A, 20);   // (w0 << 16 | w1) << 4 (low nibble unused)
+  const uint32_t yb = __funnelshift_l(B, B, 20);   // (w2 << 16 | w3) << 4
+  s[0] = y0 >> 16;
+  s[1] = __byte_perm(xc0, 0u, 0x4421);
+  s[2] = __byte_perm(y0, 0u, 0x4421);
+  s[3] = A & 0xFFFFu;
+  s[4] = ya >> 16;
+  s[5] = __byte_perm(A, 0u, 0x4403);
+  s[6] = __byte_perm(ya, 0u, 0x4421);
+  s[7] = A >> 16;
+  s[8] = y1 >> 16;
+  s[9] = __byte_perm(xc1, 0u, 0x4421);
+  s[10] = __byte_perm(y1, 0u, 0x4421);
+  s[11] = B & 0xFFFFu;
+  s[12] = yb >> 16;
+  s[13] = __byte_perm(B, 0u, 0x4403);
+  s[14] = __byte_perm(yb, 0u, 0x4421);
+  s[15] = B >> 16;
+}
+
 // Loads the 8*BITS own bytes of a thread (address 8-byte aligned for every
 // BITS, 16-byte aligned for even BITS) into 2*BITS uint32.
 template <int BITS, bool kShared>

@@ -100,6 +100,7 @@ struct FusedParams {
   int npad;       // MMA N: rows rounded up to 32, <= 128 * MTILES
   int tmem_cols;  // power of two >= 2 * npad
   int nsa;        // x' stages of npad * 128 bytes in the x' region
+  uint32_t m16;   // 16, opaque to the compiler (a multiply by it stays on the FMA pipe)
 };
 
 __device__ __forceinline__ int64_t unit_owner(int64_t z, int64_t P, int64_t TS) { return ((z + 1) * P - 1) / TS; }
@@ -395,8 +396,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       uint32_t own[2 * BITS];
       load_own_words_shared<BITS>(ring_s + s * Cfg::kSeg + lane * 8 * BITS, own);
       const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
-      Windows<BITS> win;
-      win.build(own, prev);
+      uint32_t st[4][16];
+      if constexpr (BITS == 4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) row4_states(own[2 * r], own[2 * r + 1], r == 0 ? prev : own[2 * r - 1], p.m16, st[r]);
+      } else {
+        Windows<BITS> win;
+        win.build(own, prev);
+        static_for<4>([&](auto R) {
+          static_for<16>([&](auto C) { st[R.value][C.value] = win.template state<R.value, C.value>(); });
+        });
+      }
       if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) {
         drain_from(j + 1);
         break;
@@ -405,8 +415,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       static_for<16>([&](auto C) {
         constexpr int cc = C.value;
         constexpr uint32_t cx = (uint32_t)cc << 7 | (uint32_t)(cc & 7) << 4;
-        const uint32_t lo = decode_pair_sel<false>(win.template state<0, cc>(), win.template state<1, cc>());
-        const uint32_t hi = decode_pair_sel<false>(win.template state<2, cc>(), win.template state<3, cc>());
+        const uint32_t lo = decode_pair_sel<false>(st[0][cc], st[1][cc]);
+        const uint32_t hi = decode_pair_sel<false>(st[2][cc], st[3][cc]);
         st_shared_v2(bt ^ cx, lo, hi);
       });
       fence_proxy_async_shared();  // make the generic stores visible to the tensor core
@@ -586,6 +596,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch &L, cudaStream_t st) {
   fp.smax = (int)L.plan.smax;
   fp.npad = npad;
   fp.tmem_cols = tmem_cols;
+  fp.m16 = 16u;
   fp.nsa = a_region_bytes(L.bits, MTILES) / (npad * F_BK * 2);
   if (fp.nsa > F_MAX_SA) fp.nsa = F_MAX_SA;
   cudaError_t e = MTILES == 1 ? launch_mt<1>(L.bits, tmA, fp, fp.P, st) : launch_mt<2>(L.bits, tmA, fp, fp.P, st);
