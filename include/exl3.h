@@ -252,6 +252,9 @@ exl3_status exl3_logits_masked(const void *x, int64_t M, int64_t K, const uint16
  * Synchronises `stream`, then reads and clears the current device's error
  * word. Returns EXL3_ERR_DEVICE_TIMEOUT if a kernel gave up one of its
  * bounded waits since the last read, EXL3_OK otherwise.
+ * The word is one per device, shared by every stream and workspace on it
+ * (some entry points that wait on the device have no workspace): with
+ * several streams, a timeout is reported to whichever caller reads first.
  */
 exl3_status exl3_get_device_status(void *stream);
 
