@@ -402,10 +402,13 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
       // B registers: {x'[4q], x'[4q+1]}, {x'[4q+2], x'[4q+3]} of tokens g and g + 8
       static_for<8>([&](auto J) {
         constexpr int j = J.value;
-        const uint32_t a0 = decode_pair_sel<true>(st[0][j], st[1][j]);
-        const uint32_t a1 = decode_pair_sel<true>(st[0][j + 8], st[1][j + 8]);
-        const uint32_t a2 = decode_pair_sel<true>(st[2][j], st[3][j]);
-        const uint32_t a3 = decode_pair_sel<true>(st[2][j + 8], st[3][j + 8]);
+        // pairs packed by two half-selected fp16 adds and a byte permute (measured
+        // 4 % faster at 16 rows than packing with fp16 multiply-adds, which load
+        // the half-rate fp16 pipe twice as much)
+        const uint32_t a0 = decode_pair_sel<false>(st[0][j], st[1][j]);
+        const uint32_t a1 = decode_pair_sel<false>(st[0][j + 8], st[1][j + 8]);
+        const uint32_t a2 = decode_pair_sel<false>(st[2][j], st[3][j]);
+        const uint32_t a3 = decode_pair_sel<false>(st[2][j + 8], st[3][j + 8]);
         mma16816(acc[0][j], a0, a1, a2, a3, bxv.x, bxv.y);
         mma16816(acc[1][j], a0, a1, a2, a3, bxv.z, bxv.w);
       });
