@@ -106,7 +106,7 @@ DECODE, PREFILL = 0, 1  # m_threshold values that force each path
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (128, 256, 3), (640, 384, 6), (256, 768, 2),
                                       (384, 256, 5), (256, 256, 8), (256, 384, 1), (384, 384, 7)])
-@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 16, 37])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 16, 37])
 def test_linear_decode_path(oracle, K, N, bits, M):
     m = synthetic.make_matrix(K, N, bits, seed=K + N + bits)
     x = synthetic.make_activations(M, K, seed=M)
@@ -114,6 +114,19 @@ def test_linear_decode_path(oracle, K, N, bits, M):
     y = L.linear(to_dev(x), DECODE).cpu().numpy()
     ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
     assert rel_err(y, ref) <= TOL
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_decode_small_rows_long_k(oracle, M):
+    """A long-K, wide decode-shaped layer (K=17408, N=20480): each warp's
+    slab range (about 95 slabs) streams many more chunks than its ring holds,
+    and every n-block (1088 slabs) is split over 12-13 warps' partial slots;
+    every output column against the oracle."""
+    K, N, bits = 17408, 20480, 4
+    m = synthetic.make_matrix(K, N, bits, seed=M + 40)
+    x = synthetic.make_activations(M, K, seed=M + 41)
+    y = Layer(m).linear(to_dev(x), DECODE).cpu().numpy()
+    assert rel_err(y, oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)) <= TOL
 
 
 @pytest.mark.parametrize("K,N,bits", [(512, 512, 4), (256, 384, 3), (640, 640, 6), (128, 256, 1), (384, 256, 7),

@@ -114,12 +114,15 @@ __device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const Decode
             v[mt][t][i + h] = a - b;
           }
 #pragma unroll
-      for (int s = 1; s < 8; s <<= 1)
+      for (int s = 1; s < 8; s <<= 1) {
+        // the lane's side of the butterfly: o + v or o - v, one rounding either way
+        const float sgn = (g & s) ? -1.f : 1.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float o = __shfl_xor_sync(0xffffffffu, v[mt][t][i], s * 4);
-          v[mt][t][i] = (g & s) ? (o - v[mt][t][i]) : (v[mt][t][i] + o);
+          v[mt][t][i] = fmaf(v[mt][t][i], sgn, o);
         }
+      }
     }
   const int64_t col0 = nb * 128 + 16 * g;
   float scale[16];
@@ -196,12 +199,14 @@ __device__ __forceinline__ void finalize_row(float (&v)[4], uint2 sraw, void *y,
     v[3] = a - b;
   }
 #pragma unroll
-  for (int s = 1; s < 32; s <<= 1)
+  for (int s = 1; s < 32; s <<= 1) {
+    const float sgn = (lane & s) ? -1.f : 1.f;  // o + v or o - v, one rounding either way
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
-      v[i] = (lane & s) ? (o - v[i]) : (v[i] + o);
+      v[i] = fmaf(v[i], sgn, o);
     }
+  }
   const int64_t col = nb * 128 + 4 * lane;
   const __half *sh = reinterpret_cast<const __half *>(&sraw);
   float o[4];
@@ -594,12 +599,14 @@ __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restri
           v[i + h] = a - b;
         }
 #pragma unroll
-    for (int s = 1; s < 16; s <<= 1)
+    for (int s = 1; s < 16; s <<= 1) {
+      const float sgn = (l16 & s) ? -1.f : 1.f;  // o + v or o - v, one rounding either way
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
-        v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
+        v[i] = fmaf(v[i], sgn, o);
       }
+    }
     if (valid) {
       uint32_t hb[8];
 #pragma unroll

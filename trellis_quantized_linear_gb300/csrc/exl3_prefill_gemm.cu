@@ -505,12 +505,14 @@ __global__ void __launch_bounds__(256) prefill_tail_finalize_kernel(const Prefil
           v[i + h] = a - b;
         }
 #pragma unroll
-    for (int s = 1; s < 16; s <<= 1)
+    for (int s = 1; s < 16; s <<= 1) {
+      const float sgn = (l16 & s) ? -1.f : 1.f;  // o + v or o - v, one rounding either way
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float o = __shfl_xor_sync(0xffffffffu, v[i], s);
-        v[i] = (l16 & s) ? (o - v[i]) : (v[i] + o);
+        v[i] = fmaf(v[i], sgn, o);
       }
+    }
     if (half == 1 && !second) return;
     const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.sv + col0));
     const __half *h = reinterpret_cast<const __half *>(&raw);

@@ -61,10 +61,13 @@ __global__ void __launch_bounds__(256) hadamard128_kernel(const __half *x, __hal
     }
 #pragma unroll
     for (int s = 1; s < 16; s <<= 1) {
+      // the lane's side of the butterfly, p + v or p - v, as one fma with an
+      // exact +-1 product: the same single rounding as the add or subtract
+      const float sgn = (l16 & s) ? -1.f : 1.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float p = __shfl_xor_sync(0xffffffffu, v[i], s);
-        v[i] = (l16 & s) ? (p - v[i]) : (v[i] + p);
+        const float p = __shfl_xor_sync(0xffffffffu, v[i], s);
+        v[i] = fmaf(v[i], sgn, p);
       }
     }
     if (valid) {
