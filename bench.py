@@ -181,7 +181,8 @@ class ClockSampler:
 
 
 DECODE_SOURCES = ("trellis_quantized_linear_gb300/csrc/exl3_decode_gemm.cu",
-                  "trellis_quantized_linear_gb300/csrc/exl3_common.cuh")
+                  "trellis_quantized_linear_gb300/csrc/exl3_common.cuh",
+                  "trellis_quantized_linear_gb300/csrc/exl3_bounds.cuh")
 
 
 def source_hash(*rel):

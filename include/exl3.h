@@ -73,7 +73,8 @@ typedef enum {
     EXL3_ERR_NOT_INITIALIZED = 5,    /* exl3_init was not called for the current device */
     EXL3_ERR_CUDA = 6,               /* a CUDA runtime call or a launch failed */
     EXL3_ERR_DEVICE_TIMEOUT = 7,     /* a kernel gave up a bounded wait (see exl3_get_device_status) */
-    EXL3_ERR_NOALLOC_TOO_LARGE = 8   /* the problem needs more scratch than the fixed no-alloc buffer holds */
+    EXL3_ERR_NOALLOC_TOO_LARGE = 8,  /* the problem needs more scratch than the fixed no-alloc buffer holds */
+    EXL3_ERR_OUT_OF_BOUNDS = 9       /* bounds-checked build only: a kernel's index left its buffer */
 } exl3_status;
 
 typedef enum { EXL3_F16 = 0, EXL3_F32 = 1 } exl3_dtype;
@@ -250,8 +251,10 @@ exl3_status exl3_logits_masked(const void *x, int64_t M, int64_t K, const uint16
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word. Returns EXL3_ERR_DEVICE_TIMEOUT if a kernel gave up one of its
- * bounded waits since the last read, EXL3_OK otherwise.
+ * word, which holds the first device-side error since the last read:
+ * EXL3_ERR_DEVICE_TIMEOUT if a kernel gave up one of its bounded waits,
+ * EXL3_ERR_OUT_OF_BOUNDS if a check of the bounds-checked build failed;
+ * EXL3_OK otherwise.
  * The word is one per device, shared by every stream and workspace on it
  * (some entry points that wait on the device have no workspace): with
  * several streams, a timeout is reported to whichever caller reads first.
@@ -275,6 +278,39 @@ exl3_status exl3_silu_mul(const void *gate, const void *up, void *out, int64_t n
  * counterpart; it exercises the bounded waits every pipelined kernel uses.
  */
 exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+/*
+ * Bounds-checked build. The same sources compiled with EXL3_DEBUG_BOUNDS=1
+ * give libexl3_bounds.so, with the same entry points. Before each access,
+ * its kernels check against the extents implied by the launch's arguments:
+ *   - every computed global index;
+ *   - every shared-memory address and mbarrier;
+ *   - every TMA coordinate and bulk-copy span;
+ *   - every TMEM column.
+ * A failed check skips the access (a load reads zero) and records
+ * EXL3_ERR_OUT_OF_BOUNDS in the device error word. It also prints the
+ * source line once. The check stands in for a memory checker; the pages
+ * have no counterpart to it.
+ *
+ * exl3_bounds_checked: 1 in the bounds-checked library, 0 in libexl3.so.
+ * Host only.
+ *
+ * exl3_selftest_bounds: checks that every kernel translation unit of the
+ * bounds-checked build reports to the device error word. It launches one
+ * probe kernel per unit, on `stream`. Each probe submits an index equal to
+ * its extent to the checks and touches no memory. After each probe the
+ * word is read and cleared.
+ *   *units_total   receives the number of units probed.
+ *   *units_reported receives how many recorded EXL3_ERR_OUT_OF_BOUNDS.
+ * In libexl3.so it launches nothing and sets both to 0.
+ * An error already pending in the word is returned (and cleared) before
+ * any probe runs.
+ * Synchronises `stream`.
+ * Errors: EXL3_ERR_INVALID_ARG (NULL pointer), EXL3_ERR_NOT_INITIALIZED,
+ * EXL3_ERR_CUDA.
+ */
+int exl3_bounds_checked(void);
+exl3_status exl3_selftest_bounds(int *units_reported, int *units_total, void *stream);
 
 /*
  * exl3_linear_decode_noalloc: the decode-shaped linear layer for callers

@@ -18,3 +18,17 @@ def oracle():
     import oracle as _oracle
     _oracle.build()
     return _oracle
+
+
+@pytest.fixture(autouse=True)
+def _bounds_checked_error_word(request):
+    """Under EXL3_BOUNDS_CHECKED=1 (the bounds-checked library), every GPU test
+    must leave the device error word free of bounds and timeout errors."""
+    yield
+    if os.environ.get("EXL3_BOUNDS_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    import trellis_quantized_linear_gb300 as tql
+    if tql._lib is None:
+        return
+    status = tql.exl3_get_device_status()
+    assert status not in (7, 9), f"device error word after {request.node.nodeid}: {tql.STATUS_NAMES.get(status)}"

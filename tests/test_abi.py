@@ -44,9 +44,28 @@ def test_header_declarations_are_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert tql.exl3_status_string(s)
     assert tql.exl3_status_string(99) == "unknown status"
+
+
+def test_bounds_checked_build_exports_the_same_abi(lib):
+    # The bounds-checked build compiles the same sources with EXL3_DEBUG_BOUNDS=1
+    # into its own library; it must export every declared entry point and say
+    # which build it is. No GPU call: the self-test stops at its host checks.
+    from trellis_quantized_linear_gb300 import _build
+    path = _build.build(bounds_checked=True)
+    assert os.path.basename(path) == "libexl3_bounds.so"
+    blib = ctypes.CDLL(path)
+    for name in tql.HEADER_SYMBOLS:
+        assert hasattr(blib, name), name
+    assert blib.exl3_bounds_checked() == 1
+    assert lib.exl3_bounds_checked() == 0
+    rep, tot = ctypes.c_int(-1), ctypes.c_int(-1)
+    blib.exl3_selftest_bounds.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert blib.exl3_selftest_bounds(None, ctypes.byref(tot), None) == 1  # EXL3_ERR_INVALID_ARG
+    blib.exl3_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in blib.exl3_status_string(9)
 
 
 def test_supported_bits(lib):

@@ -5,6 +5,11 @@ arguments: tensors become device pointers, the stream defaults to torch's
 current stream, and a non-zero status raises ``Exl3Error``. Every step of
 the computation runs in the library's CUDA kernels; there is no fallback. If
 ``libexl3.so`` has not been built, loading it raises immediately.
+
+With ``EXL3_BOUNDS_CHECKED=1`` in the environment the package builds and
+loads ``libexl3_bounds.so`` instead: the same kernels with every access
+checked against its launch's extents (a failed check records
+EXL3_ERR_OUT_OF_BOUNDS in the device error word).
 """
 from __future__ import annotations
 
@@ -19,11 +24,13 @@ __all__ = [
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
     "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
-    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated", "HEADER_SYMBOLS",
+    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated", "exl3_bounds_checked",
+    "exl3_selftest_bounds", "HEADER_SYMBOLS", "BOUNDS_CHECKED",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libexl3.so")
+BOUNDS_CHECKED = os.environ.get("EXL3_BOUNDS_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_PKG, "libexl3_bounds.so" if BOUNDS_CHECKED else "libexl3.so")
 
 EXL3_F16 = 0
 EXL3_F32 = 1
@@ -35,7 +42,7 @@ EXL3_NOALLOC_SCRATCH_BYTES = 24 << 20
 STATUS_NAMES = {
     0: "EXL3_OK", 1: "EXL3_ERR_INVALID_ARG", 2: "EXL3_ERR_ALIGNMENT", 3: "EXL3_ERR_UNSUPPORTED_BITS",
     4: "EXL3_ERR_WORKSPACE_TOO_SMALL", 5: "EXL3_ERR_NOT_INITIALIZED", 6: "EXL3_ERR_CUDA",
-    7: "EXL3_ERR_DEVICE_TIMEOUT", 8: "EXL3_ERR_NOALLOC_TOO_LARGE",
+    7: "EXL3_ERR_DEVICE_TIMEOUT", 8: "EXL3_ERR_NOALLOC_TOO_LARGE", 9: "EXL3_ERR_OUT_OF_BOUNDS",
 }
 
 # Every function include/exl3.h declares.
@@ -45,7 +52,8 @@ HEADER_SYMBOLS = (
     "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct", "exl3_linear",
     "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
     "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
-    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated",
+    "exl3_weight_rotated_workspace_bytes", "exl3_linear_weight_rotated", "exl3_bounds_checked",
+    "exl3_selftest_bounds",
 )
 
 
@@ -63,13 +71,14 @@ _vp = ctypes.c_void_p
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles libexl3.so for sm_103a with nvcc (in-tree)."""
+    """Compiles the library this process loads (libexl3.so, or libexl3_bounds.so
+    under EXL3_BOUNDS_CHECKED=1) for sm_103a with nvcc (in-tree)."""
     from . import _build
-    return _build.build(force=force, verbose=verbose)
+    return _build.build(force=force, verbose=verbose, bounds_checked=BOUNDS_CHECKED)
 
 
 def load():
-    """Loads libexl3.so; raises if it has not been built."""
+    """Loads the library (LIB_PATH); raises if it has not been built."""
     global _lib
     with _lock:
         if _lib is not None:
@@ -103,6 +112,8 @@ def load():
             "exl3_weight_rotated_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
             "exl3_linear_weight_rotated": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _i64, _i64, _vp, _vp,
                                                           _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]),
+            "exl3_bounds_checked": (ctypes.c_int, []),
+            "exl3_selftest_bounds": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -239,6 +250,20 @@ def exl3_get_device_status(stream=None) -> int:
 def exl3_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Launches the bounded-wait self-test kernel (see include/exl3.h)."""
     _check(load().exl3_selftest_wait_timeout(int(limit_us), _stream(stream)), "exl3_selftest_wait_timeout")
+
+
+def exl3_bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return load().exl3_bounds_checked() == 1
+
+
+def exl3_selftest_bounds(stream=None) -> tuple[int, int]:
+    """Runs the bounds-check reporting self-test (see include/exl3.h); returns
+    (units that reported, units probed): (6, 6) in the bounds-checked build,
+    (0, 0) in libexl3.so."""
+    rep, tot = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().exl3_selftest_bounds(ctypes.byref(rep), ctypes.byref(tot), _stream(stream)), "exl3_selftest_bounds")
+    return rep.value, tot.value
 
 
 def exl3_linear_decode_noalloc(x, M: int, K: int, trellis, bits: int, n_stored: int, n_gemm: int, su, sv, y,

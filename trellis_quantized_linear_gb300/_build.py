@@ -2,8 +2,11 @@
 
 Each translation unit is compiled in parallel; objects go to
 ``trellis_quantized_linear_gb300/_build/`` and the shared library to
-``trellis_quantized_linear_gb300/libexl3.so``. A rebuild happens only when a
-source or header is newer than the library.
+``trellis_quantized_linear_gb300/libexl3.so``. With ``bounds_checked`` the
+same sources are compiled with ``EXL3_DEBUG_BOUNDS=1`` (every kernel access
+checked against its launch's extents) into ``_build_bounds/`` and
+``libexl3_bounds.so``. A rebuild happens only when a source or header is
+newer than the library.
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libexl3.so")
+BUILD_BOUNDS = os.path.join(PKG, "_build_bounds")
+LIB_BOUNDS = os.path.join(PKG, "libexl3_bounds.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -37,25 +42,28 @@ def _inputs() -> list[str]:
         [os.path.join(ROOT, "include", "exl3.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, bounds_checked: bool = False) -> str:
+    lib, build_dir = (LIB_BOUNDS, BUILD_BOUNDS) if bounds_checked else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     common = [nvcc, "-std=c++17", ARCH, "-O3", "-lineinfo", "-Xcompiler", "-fPIC",
               "-I", os.path.join(ROOT, "include")]
+    if bounds_checked:
+        common += ["-DEXL3_DEBUG_BOUNDS=1"]
     if verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
         r = subprocess.run(common + ["-c", src, "-o", obj], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -66,15 +74,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, ARCH, "-shared", "-o", tmp] + objs + ["-lcudart_static", "-lrt", "-ldl", "-lpthread"],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, bounds_checked="--bounds" in sys.argv))

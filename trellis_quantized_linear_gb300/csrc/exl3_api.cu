@@ -11,7 +11,8 @@
 #include "exl3_common.cuh"
 #include "exl3_internal.h"
 
-// Device error word: kernels set it when they give up a bounded wait.
+// Device error word: kernels record in it the first bounded wait they gave
+// up (and, in the bounds-checked build, the first failed bounds check).
 __device__ int g_exl3_status_word;
 
 namespace exl3 {
@@ -213,10 +214,10 @@ exl3_status exl3_init(int device) {
   if (cudaGetSymbolAddress(&status, g_exl3_status_word) != cudaSuccess) return EXL3_ERR_CUDA;
   info.status = static_cast<int *>(status);
   if (cudaMemset(info.status, 0, sizeof(int)) != cudaSuccess) return EXL3_ERR_CUDA;
-  if (init_rotate_kernels() != cudaSuccess || init_reconstruct_kernels() != cudaSuccess ||
-      init_reconstruct_rotated_kernels() != cudaSuccess ||
-      init_decode_kernels() != cudaSuccess || init_prefill_kernels() != cudaSuccess ||
-      init_fused_kernels() != cudaSuccess)
+  if (init_rotate_kernels(info.status) != cudaSuccess || init_reconstruct_kernels(info.status) != cudaSuccess ||
+      init_reconstruct_rotated_kernels(info.status) != cudaSuccess ||
+      init_decode_kernels(info.status) != cudaSuccess || init_prefill_kernels(info.status) != cudaSuccess ||
+      init_fused_kernels(info.status) != cudaSuccess)
     return EXL3_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return EXL3_ERR_CUDA;
   info.ready = true;
@@ -235,6 +236,7 @@ const char *exl3_status_string(int status) {
     case EXL3_ERR_CUDA: return "CUDA runtime error or failed launch";
     case EXL3_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on the device";
     case EXL3_ERR_NOALLOC_TOO_LARGE: return "problem needs more scratch than the fixed no-alloc buffer holds";
+    case EXL3_ERR_OUT_OF_BOUNDS: return "a bounds check of the bounds-checked build failed on the device";
     default: return "unknown status";
   }
 }
@@ -416,6 +418,35 @@ exl3_status exl3_selftest_wait_timeout(uint32_t limit_us, void *stream) {
   if (!dev) return EXL3_ERR_NOT_INITIALIZED;
   return from_cuda(launch_wait_timeout_selftest(dev->status, (unsigned long long)limit_us * 1000ull,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int exl3_bounds_checked(void) { return EXL3_DEBUG_BOUNDS ? 1 : 0; }
+
+exl3_status exl3_selftest_bounds(int *units_reported, int *units_total, void *stream) {
+  if (!units_reported || !units_total) return EXL3_ERR_INVALID_ARG;
+  *units_reported = 0;
+  *units_total = 0;
+  const DeviceInfo *dev = current_device();
+  if (!dev) return EXL3_ERR_NOT_INITIALIZED;
+#if EXL3_DEBUG_BOUNDS
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // An error recorded before the self-test is returned (and cleared) first.
+  const exl3_status pending = exl3_get_device_status(stream);
+  if (pending != EXL3_OK) return pending;
+  cudaError_t (*const probes[])(cudaStream_t) = {bounds_probe_rotate,  bounds_probe_decode,
+                                                 bounds_probe_fused,   bounds_probe_prefill,
+                                                 bounds_probe_reconstruct, bounds_probe_reconstruct_rotated};
+  for (auto *probe : probes) {
+    ++*units_total;
+    if (probe(st) != cudaSuccess) return EXL3_ERR_CUDA;
+    const exl3_status s = exl3_get_device_status(stream);
+    if (s == EXL3_ERR_OUT_OF_BOUNDS) ++*units_reported;
+    else if (s != EXL3_OK) return s;
+  }
+#else
+  (void)stream;
+#endif
+  return EXL3_OK;
 }
 
 exl3_status exl3_get_device_status(void *stream) {

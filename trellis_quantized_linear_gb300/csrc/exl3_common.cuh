@@ -8,6 +8,7 @@
 #include <utility>
 
 #include "../../include/exl3.h"
+#include "exl3_bounds.cuh"
 
 namespace exl3 {
 
@@ -284,8 +285,9 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// The error word keeps the first error since it was last read.
 __device__ __forceinline__ void report_timeout(int *status) {
-  if (status) atomicExch(status, (int)EXL3_ERR_DEVICE_TIMEOUT);
+  if (status) atomicCAS(status, 0, (int)EXL3_ERR_DEVICE_TIMEOUT);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

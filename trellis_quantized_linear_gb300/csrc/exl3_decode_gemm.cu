@@ -125,12 +125,13 @@ __device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const Decode
       }
     }
   const int64_t col0 = nb * 128 + 16 * g;
+  const bool cols_ok = EXL3_SPAN(col0, 16, p.n_gemm);
   float scale[16];
   {
     const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
 #pragma unroll
     for (int a = 0; a < 2; ++a) {
-      const uint4 raw = __ldg(svp + a);
+      const uint4 raw = cols_ok ? __ldg(svp + a) : uint4{};
       const __half *h = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
       for (int e = 0; e < 8; ++e) scale[8 * a + e] = __half2float(h[e]) * kInvSqrt128;
@@ -144,7 +145,7 @@ __device__ __forceinline__ void finish_block(float (&v)[MT][2][16], const Decode
       float o[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) o[c] = (col0 + c < p.n_valid) ? v[mt][t][c] * scale[c] : -INFINITY;
-      if (m < p.rows) {
+      if (m < p.rows && cols_ok) {
         if (p.y_f32) {
           float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + (int64_t)m * p.n_gemm + col0);
 #pragma unroll
@@ -172,15 +173,16 @@ __device__ __forceinline__ int64_t slab_owner(int64_t z, int64_t P, int64_t TS) 
 // sv is a weight, not an output of the GEMM: a kernel that waits for the
 // GEMM loads it before the wait, off the critical path (after a long decode
 // it has usually left L2).
-__device__ __forceinline__ uint2 load_sv4(const __half *__restrict__ sv, int64_t nb, int lane) {
-  return __ldg(reinterpret_cast<const uint2 *>(sv + nb * 128 + 4 * lane));
+__device__ __forceinline__ uint2 load_sv4(const __half *__restrict__ sv, int64_t nb, int lane, int64_t n_gemm) {
+  return EXL3_SPAN(nb * 128 + 4 * lane, 4, n_gemm) ? __ldg(reinterpret_cast<const uint2 *>(sv + nb * 128 + 4 * lane))
+                                                    : uint2{};
 }
 
 // Output rotation (had_r_128 over the 128 columns spread as 4 per lane), sv
 // (the lane's four values from load_sv4), mask and store of one row of
 // n-block nb.
 __device__ __forceinline__ void finalize_row(float (&v)[4], uint2 sraw, void *y, int y_f32, int64_t n_gemm,
-                                             int64_t n_valid, int64_t nb, int m, int lane) {
+                                             int64_t n_valid, int64_t nb, int m, int rows, int lane) {
   {
     float a = v[0], b = v[1];
     v[0] = a + b;
@@ -212,6 +214,7 @@ __device__ __forceinline__ void finalize_row(float (&v)[4], uint2 sraw, void *y,
   float o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) o[i] = (col + i < n_valid) ? v[i] * (__half2float(sh[i]) * kInvSqrt128) : -INFINITY;
+  if (!EXL3_RANGE(m, 0, rows) || !EXL3_SPAN(col, 4, n_gemm)) return;
   if (y_f32) {
     *reinterpret_cast<float4 *>(static_cast<float *>(y) + (int64_t)m * n_gemm + col) = make_float4(o[0], o[1], o[2], o[3]);
   } else {
@@ -280,6 +283,8 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
   uint8_t *ring = smem + warp * Cfg::kWarpRing;
   const uint32_t ring_s = smem_u32(ring);
   const uint32_t bar0 = smem_u32(smem + Cfg::kWarps * Cfg::kWarpRing) + warp * R * 8;
+  // this warp's ring and barriers inside the CTA's shared memory (warp-uniform)
+  if (!EXL3_SMEM(ring_s, Cfg::kWarpRing) || !EXL3_SMEM(bar0, 8 * R)) return;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -297,12 +302,19 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     const int len = chunk_len(i_tk, i_z);
     const uint32_t bar = bar0 + 8 * i_st;
     mbar_arrive_expect_tx(bar, CHK * Cfg::kSeg + len * kXFrag);
-    tma_load_2d_u64(ring_s + i_st * Cfg::kStage, &tmap, bar, i_nb * (32 * BITS), i_tk);
+    // box: 8-byte columns [32*BITS*i_nb, +32*BITS) (an even start: the
+    // 16-byte rule), rows [i_tk, +CHK) of KT (rows past KT read zero)
+    if (EXL3_RANGE(i_nb, 0, p.n_gemm / 128) && EXL3_RANGE(i_tk, 0, KT) && EXL3_RANGE(len, 1, CHK + 1) &&
+        EXL3_ALIGNED(i_nb * (32 * BITS) * 8, 16) && EXL3_RANGE(i_st, 0, R))
+      tma_load_2d_u64(ring_s + i_st * Cfg::kStage, &tmap, bar, i_nb * (32 * BITS), i_tk);
     return len;
   };
   auto issue_x = [&](int st, int tk, int len) {
-    bulk_g2s(ring_s + st * Cfg::kStage + CHK * Cfg::kSeg, p.xf + (size_t)tk * kXFrag, len * kXFrag,
-             bar0 + 8 * st);
+    const uint32_t dst = ring_s + st * Cfg::kStage + CHK * Cfg::kSeg;
+    if (EXL3_SPAN((int64_t)tk * kXFrag, len * kXFrag, (int64_t)KT * kXFrag) &&
+        EXL3_SPAN(dst - ring_s, len * kXFrag, Cfg::kWarpRing) && EXL3_ALIGNED(dst, 16) &&
+        EXL3_ALIGNED(reinterpret_cast<uintptr_t>(p.xf + (size_t)tk * kXFrag), 16))
+      bulk_g2s(dst, p.xf + (size_t)tk * kXFrag, len * kXFrag, bar0 + 8 * st);
   };
   auto advance = [&](int len) {
     i_z += len;
@@ -363,13 +375,16 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
       // sums the n-block's slots in slot order
       const int64_t pf = slab_owner((int64_t)cnb * KT, p.P, p.TS);
       const int64_t slot_elems = (int64_t)8 * MT * 128;
+      // slot pw - pf of the n-block's smax, row m of the slot's 8 * MT
+      const bool slot_ok = EXL3_RANGE(cnb, 0, p.n_gemm / 128) && EXL3_RANGE(pw - pf, 0, p.smax) &&
+                           EXL3_SPAN(16 * g, 16, 128);
       float *part = p.partials + ((int64_t)cnb * p.smax + (pw - pf)) * slot_elems;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
           const int m = 8 * mt + 2 * q + tt;
-          if (m < p.rows) {
+          if (m < p.rows && slot_ok && EXL3_RANGE(m, 0, 8 * MT)) {
             float4 *dst = reinterpret_cast<float4 *>(part + m * 128 + 16 * g);
             dst[0] = make_float4(acc[mt][0][tt], acc[mt][1][tt], acc[mt][2][tt], acc[mt][3][tt]);
             dst[1] = make_float4(acc[mt][4][tt], acc[mt][5][tt], acc[mt][6][tt], acc[mt][7][tt]);
@@ -389,8 +404,15 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
   // the lane's 16 bytes of x' fragments for the slab.
   auto slab = [&](const uint8_t *tr, const uint8_t *xb) {
     uint32_t own[2 * BITS];
-    load_own_words<BITS, true>(tr + lane * 8 * BITS, own);
-    const uint4 bxv = *reinterpret_cast<const uint4 *>(xb + lane * 16);
+    if (EXL3_SPAN(smem_u32(tr + lane * 8 * BITS) - ring_s, 8 * BITS, Cfg::kWarpRing)) {
+      load_own_words<BITS, true>(tr + lane * 8 * BITS, own);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * BITS; ++i) own[i] = 0;
+    }
+    const uint4 bxv = EXL3_SPAN(smem_u32(xb + lane * 16) - ring_s, 16, Cfg::kWarpRing)
+                          ? *reinterpret_cast<const uint4 *>(xb + lane * 16)
+                          : uint4{};
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
     uint32_t st[4][16];
     slab_states<BITS>(own, prev, p.m16, st);
@@ -492,12 +514,14 @@ __global__ void __launch_bounds__(256) decode_finalize_kernel(const float *__res
   const int64_t pf = slab_owner(nb * KT, P, TS);
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
   if (cnt == 1 && !all_blocks) return;  // finished by its single owner
-  const uint2 s4 = load_sv4(sv, nb, lane);
+  const uint2 s4 = load_sv4(sv, nb, lane, n_gemm);
   wait_prior_grid();  // partial slots come from the decode kernel
   const float *base = partials + nb * smax * slot_elems + m * 128 + 4 * lane;
+  // cnt of the n-block's smax slots; the lane's columns of row m in a slot
+  const bool ok = EXL3_RANGE(cnt, 1, smax + 1) && EXL3_SPAN(m * 128 + 4 * lane, 4, slot_elems);
   float v[4];
-  sum_slots(base, cnt, slot_elems, v);
-  finalize_row(v, s4, y, y_f32, n_gemm, n_valid, nb, m, lane);
+  sum_slots(base, ok ? cnt : 0, slot_elems, v);
+  finalize_row(v, s4, y, y_f32, n_gemm, n_valid, nb, m, rows, lane);
 }
 
 // The same reduction for the fused tensor-core GEMM (up to 256 rows, 2-3
@@ -519,14 +543,17 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
   if (nb >= n_gemm / 128) return;
   const int64_t pf = slab_owner(nb * KT, P, TS);
   const int cnt = (int)(slab_owner((nb + 1) * KT - 1, P, TS) - pf + 1);
-  const uint2 s4 = load_sv4(sv, nb, lane);
+  const uint2 s4 = load_sv4(sv, nb, lane, n_gemm);
   wait_prior_grid();  // partial slots come from the GEMM kernel
   const float *base = partials + nb * smax * slot_elems + (int64_t)m0 * 128 + 4 * lane;
   const int nr = rows - m0 < RPW ? rows - m0 : RPW;
+  // cnt of the n-block's smax slots; rows m0 .. m0 + nr - 1 of a slot
+  const bool ok = EXL3_RANGE(cnt, 1, smax + 1) && EXL3_RANGE(nr, 1, RPW + 1) &&
+                  EXL3_SPAN((int64_t)(m0 + nr - 1) * 128 + 4 * lane, 4, slot_elems);
   float v[RPW][4];
 #pragma unroll
   for (int r = 0; r < RPW; ++r) v[r][0] = v[r][1] = v[r][2] = v[r][3] = 0.f;
-  for (int s0 = 0; s0 < cnt; s0 += SC) {
+  for (int s0 = 0; s0 < (ok ? cnt : 0); s0 += SC) {
     float4 f[SC][RPW];
 #pragma unroll
     for (int s = 0; s < SC; ++s)
@@ -548,7 +575,7 @@ __global__ void __launch_bounds__(256) fused_finalize_kernel(const float *__rest
   }
 #pragma unroll
   for (int r = 0; r < RPW; ++r)
-    if (r < nr) finalize_row(v[r], s4, y, y_f32, n_gemm, n_valid, nb, m0 + r, lane);
+    if (r < nr) finalize_row(v[r], s4, y, y_f32, n_gemm, n_valid, nb, m0 + r, rows, lane);
 }
 
 // x' = RNE_fp16(had_r_128(x * su)) for up to 8*MT rows, in fragment order:
@@ -579,8 +606,9 @@ __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restri
     float v[8];
     if (valid && m < rows) {
       const int64_t k = kb * 128 + 8 * l16;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + k));
-      const uint4 sraw = __ldg(reinterpret_cast<const uint4 *>(su + k));
+      const bool ok = EXL3_SPAN((int64_t)m * K + k, 8, (int64_t)rows * K) && EXL3_SPAN(k, 8, K);
+      const uint4 raw = ok ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + k)) : uint4{};
+      const uint4 sraw = ok ? __ldg(reinterpret_cast<const uint4 *>(su + k)) : uint4{};
       const __half *h = reinterpret_cast<const __half *>(&raw);
       const __half *sh = reinterpret_cast<const __half *>(&sraw);
 #pragma unroll
@@ -615,14 +643,19 @@ __global__ void __launch_bounds__(256) rotate_frag_kernel(const __half *__restri
       // 8*(l16&1) .. +7, i.e. lanes q = 2*(l16&1) and q + 1 of group m & 7
       const int64_t tk = kb * 8 + (l16 >> 1);
       const int qq = 2 * (l16 & 1);
-      uint8_t *d0 = xf + (tk * 32 + (m & 7) * 4 + qq) * 16;
+      const int64_t xo = (tk * 32 + (m & 7) * 4 + qq) * 16;  // K/16 slabs of 512 bytes
+      uint8_t *d0 = xf + xo;
       if constexpr (MT == 1) {
-        *reinterpret_cast<uint4 *>(d0) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-        *reinterpret_cast<uint4 *>(d0 + 16) = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        if (EXL3_SPAN(xo, 32, K * 32)) {
+          *reinterpret_cast<uint4 *>(d0) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+          *reinterpret_cast<uint4 *>(d0 + 16) = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        }
       } else {
         const int off = (m >> 3) * 8;
-        *reinterpret_cast<uint2 *>(d0 + off) = make_uint2(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16);
-        *reinterpret_cast<uint2 *>(d0 + 16 + off) = make_uint2(hb[4] | hb[5] << 16, hb[6] | hb[7] << 16);
+        if (EXL3_RANGE(m, 0, 16) && EXL3_SPAN(xo + off, 24, K * 32)) {
+          *reinterpret_cast<uint2 *>(d0 + off) = make_uint2(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16);
+          *reinterpret_cast<uint2 *>(d0 + 16 + off) = make_uint2(hb[4] | hb[5] << 16, hb[6] | hb[7] << 16);
+        }
       }
     }
   }
@@ -730,8 +763,9 @@ size_t decode_partials_bytes(const DecodePlan &plan, int64_t n_blocks) {
   return a > b ? a : b;
 }
 
-cudaError_t init_decode_kernels() {
-  cudaError_t e;
+cudaError_t init_decode_kernels(int *status) {
+  cudaError_t e = EXL3_BIND_BOUNDS_WORD(status);
+  if (e != cudaSuccess) return e;
   if ((e = init_bits<1>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
@@ -804,5 +838,9 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   return launch_decode_finalize(L.partials, dp.smax, (int64_t)8 * MT * 128, L.sv, L.y, L.y_f32, L.n_gemm, L.n_valid,
                                 L.rows, dp.P, dp.TS, dp.KT, /*all_blocks=*/0, st);
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_decode(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3

@@ -150,6 +150,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   const int64_t zs = c * p.TS / p.P, ze = (c + 1) * p.TS / p.P;
   const int len = (int)(ze - zs);
   const int KS = p.KS;
+  // The layout inside the CTA's shared memory, the x' stages inside their
+  // region, the MMA width and the TMEM allocation (CTA-uniform: checked
+  // before any barrier or TMEM is set up).
+  if (!EXL3_SMEM(smem_s, Cfg::kOffBar + Cfg::kNumBars * 8 + 4) || !EXL3_RANGE(nsa, 1, F_SA + 1) ||
+      !EXL3_SPAN(0, nsa * a_stage, Cfg::kARegion) || !EXL3_RANGE(p.npad, 32, 128 * MTILES + 1) ||
+      !EXL3_ALIGNED(p.npad, 32) || !EXL3_SPAN(0, 2 * p.npad, p.tmem_cols) || !EXL3_RANGE(p.tmem_cols, 32, 513))
+    return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nsa; ++s) {
@@ -191,7 +198,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       if (!warp_wait(a_empty(as), aph ^ 1u, p.status)) break;
       if (leader) {
         mbar_arrive_expect_tx(a_full(as), a_stage);
-        tma_load_2d(smem_s + as * a_stage, &tmA, a_full(as), ks * F_BK, 0);
+        // box: fp16 columns [64 ks, +64) (128 bytes: the 16-byte rule), rows
+        // [0, npad); the stage 1024-byte aligned for the 128-byte swizzle
+        if (EXL3_RANGE(ks, 0, KS) && EXL3_RANGE(as, 0, nsa) && EXL3_ALIGNED(smem_s + as * a_stage, 1024))
+          tma_load_2d(smem_s + as * a_stage, &tmA, a_full(as), ks * F_BK, 0);
       }
       __syncwarp();
       ++issued;
@@ -242,10 +252,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         const uint64_t xdesc = sw128_desc(smem_s + as * a_stage);
         const uint32_t d = tmem_base + (uint32_t)(ab * p.npad);
         if (leader) {
+          // operand stages and the accumulator's npad TMEM columns
+          const bool ok = EXL3_RANGE(as, 0, nsa) && EXL3_RANGE(bs, 0, F_SB) &&
+                          EXL3_SPAN(ab * p.npad, p.npad, p.tmem_cols);
 #pragma unroll
           for (int k16 = 0; k16 < F_BK / 16; ++k16)
-            tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
-                   (!first || k16 > 0) ? 1u : 0u);
+            if (ok)
+              tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
+                     (!first || k16 > 0) ? 1u : 0u);
           tc_commit(a_empty(as));
           tc_commit(b_empty(bs));
           if (last) tc_commit(acc_full(ab));
@@ -312,10 +326,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             const bool last = (kk + t == len - 1) || (k2 == KS - 1);
             const uint64_t wdesc = sw128_desc(smem_s + Cfg::kOffB + b * F_B_STAGE);
             const uint64_t xdesc = sw128_desc(smem_s + a * a_stage);
+            const bool ok = EXL3_RANGE(a, 0, nsa) && EXL3_RANGE(b, 0, F_SB) &&
+                            EXL3_SPAN(ab * p.npad, p.npad, p.tmem_cols);
 #pragma unroll
             for (int k16 = 0; k16 < F_BK / 16; ++k16)
-              tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
-                     (!first || k16 > 0) ? 1u : 0u);
+              if (ok)
+                tc_mma(d, wdesc + (uint64_t)(2 * k16), xdesc + (uint64_t)(2 * k16), idesc,
+                       (!first || k16 > 0) ? 1u : 0u);
             tc_commit(a_empty(a));
             tc_commit(b_empty(b));
             if (last) tc_commit(acc_full(ab));
@@ -372,8 +389,11 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       }
       const int s = j % F_RD;
       mbar_arrive_expect_tx(dec_full(dw, s), Cfg::kSeg);
-      bulk_g2s(ring_s + s * Cfg::kSeg, p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS), Cfg::kSeg,
-               dec_full(dw, s));
+      // the slab's 8 tiles: tile row tk of the 4 KS, tiles [8 nb, +8) of tiles_n
+      if (EXL3_RANGE(tk, 0, 4 * (int64_t)KS) && EXL3_RANGE(nb, 0, p.n_gemm / 128) &&
+          EXL3_SPAN(nb * 8, 8, p.tiles_n) && EXL3_ALIGNED((tk * p.tiles_n + nb * 8) * (32 * BITS), 16))
+        bulk_g2s(ring_s + s * Cfg::kSeg, p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS), Cfg::kSeg,
+                 dec_full(dw, s));
       ++issued;
     };
     if (lane == 0)
@@ -394,7 +414,12 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         break;
       }
       uint32_t own[2 * BITS];
-      load_own_words_shared<BITS>(ring_s + s * Cfg::kSeg + lane * 8 * BITS, own);
+      if (EXL3_SPAN(s * Cfg::kSeg + lane * 8 * BITS, 8 * BITS, F_RD * Cfg::kSeg)) {
+        load_own_words_shared<BITS>(ring_s + s * Cfg::kSeg + lane * 8 * BITS, own);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2 * BITS; ++i) own[i] = 0;
+      }
       const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
       uint32_t st[4][16];
       if constexpr (BITS == 4) {
@@ -417,7 +442,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         constexpr uint32_t cx = (uint32_t)cc << 7 | (uint32_t)(cc & 7) << 4;
         const uint32_t lo = decode_pair_sel<false>(st[0][cc], st[1][cc]);
         const uint32_t hi = decode_pair_sel<false>(st[2][cc], st[3][cc]);
-        st_shared_v2(bt ^ cx, lo, hi);
+        if (EXL3_RANGE(bs, 0, F_SB) && EXL3_SPAN((bt ^ cx) - (smem_s + Cfg::kOffB + bs * F_B_STAGE), 8, F_B_STAGE))
+          st_shared_v2(bt ^ cx, lo, hi);
       });
       fence_proxy_async_shared();  // make the generic stores visible to the tensor core
       __syncwarp();
@@ -447,14 +473,23 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       float *slot = p.partials + (nb * p.smax + (c - pf)) * (int64_t)(MTILES * 128 * 128) + 16 * (i >> 4) +
                     ((i & 15) ^ (i >> 4));
       const uint32_t taddr = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(ab * p.npad);
+      // slot c - pf of the n-block's smax, rows < 128 * MTILES of the slot
+      const bool slot_ok = EXL3_RANGE(nb, 0, p.n_gemm / 128) && EXL3_RANGE(c - pf, 0, p.smax) &&
+                           EXL3_RANGE(p.rows, 1, 128 * MTILES + 1);
 #pragma unroll 1
       for (int m0 = 0; m0 < p.rows; m0 += 32) {
         float t[32];
-        tmem_ld32(taddr + m0, t);
-        if (m0 + 32 <= p.rows) {
+        // 32 TMEM columns inside this accumulator (warp-uniform)
+        if (EXL3_SPAN(ab * p.npad + m0, 32, p.tmem_cols) && EXL3_SPAN(m0, 32, p.npad)) {
+          tmem_ld32(taddr + m0, t);
+        } else {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) t[r] = 0.f;
+        }
+        if (slot_ok && m0 + 32 <= p.rows) {
 #pragma unroll
           for (int r = 0; r < 32; ++r) slot[(int64_t)(m0 + r) * 128] = t[r];
-        } else {
+        } else if (slot_ok) {
 #pragma unroll
           for (int r = 0; r < 32; ++r)
             if (m0 + r < p.rows) slot[(int64_t)(m0 + r) * 128] = t[r];
@@ -557,8 +592,9 @@ size_t fused_partials_bytes(const FusedPlan &f, int64_t n_blocks) {
   return (size_t)n_blocks * f.smax * 256 * 128 * 4;
 }
 
-cudaError_t init_fused_kernels() {
-  cudaError_t e;
+cudaError_t init_fused_kernels(int *status) {
+  cudaError_t e = EXL3_BIND_BOUNDS_WORD(status);
+  if (e != cudaSuccess) return e;
   if ((e = init_bits<1>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
@@ -604,5 +640,9 @@ cudaError_t launch_fused_gemm(const FusedLaunch &L, cudaStream_t st) {
   return launch_decode_finalize(L.partials, fp.smax, (int64_t)MTILES * 128 * 128, L.sv, L.y, L.y_f32, L.n_gemm,
                                 L.n_valid, L.rows, fp.P, fp.TS, fp.KS, /*all_blocks=*/1, st);
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_fused(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3

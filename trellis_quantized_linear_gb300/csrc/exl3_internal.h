@@ -106,21 +106,33 @@ struct FusedLaunch {
   FusedPlan plan;
 };
 
-cudaError_t init_rotate_kernels();
-cudaError_t init_fused_kernels();
+// Each kernel translation unit's set-up; `status` is the device error word
+// (bound into the unit's bounds checks in the bounds-checked build).
+cudaError_t init_rotate_kernels(int *status);
+cudaError_t init_fused_kernels(int *status);
 cudaError_t launch_fused_gemm(const FusedLaunch &p, cudaStream_t st);
 // Sums the partial slots of shared n-blocks (slot order), output rotation,
 // sv, mask, store. Units are k slabs (decode GEMM) or k steps (fused GEMM).
 cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t slot_elems, const void *sv, void *y,
                                    int y_f32, int64_t n_gemm, int64_t n_valid, int rows, int64_t P, int64_t TS,
                                    int units_per_block, int all_blocks, cudaStream_t st);
-cudaError_t init_reconstruct_kernels();
-cudaError_t init_reconstruct_rotated_kernels();
+cudaError_t init_reconstruct_kernels(int *status);
+cudaError_t init_reconstruct_rotated_kernels(int *status);
 cudaError_t launch_reconstruct_rotated(const uint16_t *trellis, int bits, int64_t K, int64_t n_stored, int64_t n0,
                                        int64_t n_cols, const void *su, const void *sv, void *w, int layout,
                                        cudaStream_t st);
-cudaError_t init_decode_kernels();
-cudaError_t init_prefill_kernels();
+cudaError_t init_decode_kernels(int *status);
+cudaError_t init_prefill_kernels(int *status);
+
+#if EXL3_DEBUG_BOUNDS
+// One probe launch per kernel translation unit (exl3_selftest_bounds).
+cudaError_t bounds_probe_rotate(cudaStream_t st);
+cudaError_t bounds_probe_decode(cudaStream_t st);
+cudaError_t bounds_probe_fused(cudaStream_t st);
+cudaError_t bounds_probe_prefill(cudaStream_t st);
+cudaError_t bounds_probe_reconstruct(cudaStream_t st);
+cudaError_t bounds_probe_reconstruct_rotated(cudaStream_t st);
+#endif
 
 cudaError_t launch_hadamard128(const void *x, void *y, const void *pre, int64_t rows, int64_t cols,
                                int num_sms, cudaStream_t st);

@@ -112,6 +112,7 @@ struct WorkIter {
 // In-register orthonormal had_r_128 of one row block, then * sv, mask, store
 // (rotation and sv skipped for a pre-rotated weight).
 __device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillParams &p, int64_t row, int col0) {
+  const bool cols_ok = EXL3_SPAN(col0, 128, p.nc);  // sv and y columns of this chunk
   if (p.rotate) {
 #pragma unroll
     for (int h = 1; h < 128; h <<= 1) {
@@ -127,7 +128,7 @@ __device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillPar
     const uint4 *svp = reinterpret_cast<const uint4 *>(p.sv + col0);
 #pragma unroll
     for (int a = 0; a < 16; ++a) {
-      uint4 raw = __ldg(svp + a);
+      const uint4 raw = cols_ok ? __ldg(svp + a) : uint4{};
       const __half *h = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -136,7 +137,7 @@ __device__ __forceinline__ void epilogue_block(float (&v)[128], const PrefillPar
       }
     }
   }
-  if (row >= p.M) return;
+  if (row >= p.M || !cols_ok) return;
   if (p.y_f32) {
     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + row * p.ldy + col0);
 #pragma unroll
@@ -178,6 +179,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kblocks = p.K / BK;
   const int ntiles = p.dp_tiles;  // whole tiles of a data-parallel launch
+  // ring, barriers and TMEM slot inside the CTA's shared memory (CTA-uniform,
+  // before any barrier or TMEM is set up)
+  if (!EXL3_SMEM(smem_s, RING_BYTES + (2 * STAGES + 5) * 8 + 4)) return;
+  // A tile (tm, tn, kb): TMA boxes at fp16 column 64 kb (128 bytes: the
+  // 16-byte rule), A rows 128 tm of the rotated rows, B rows 256 tn of the
+  // chunk; both inside the problem.
+  auto tile_ok = [&](int tm, int tn, int kb) {
+    return EXL3_RANGE(tm, 0, p.tiles_m) && EXL3_RANGE(tn, 0, p.tiles_n) && EXL3_RANGE(kb, 0, kblocks) &&
+           EXL3_ALIGNED(kb * BK * 2, 16);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -219,8 +230,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
-          tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
-          tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          if (tile_ok(tm, tn, kb)) {
+            tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
+            tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -248,8 +261,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
-          tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
-          tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          if (tile_ok(tm, tn, kb)) {
+            tma_load_2d(a_s(stage), &tmA, full_bar(stage), kb * BK, tm * BM);
+            tma_load_2d(b_s(stage), &tmB, full_bar(stage), kb * BK, tn * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -286,7 +301,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle atom
-            tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
+            if (EXL3_RANGE(acc, 0, 2))  // 256 columns of the 512 allocated
+              tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -325,7 +341,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle atom
-            tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb != w.kb0 || kk != 0));
+            if (EXL3_RANGE(acc, 0, 2))
+              tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb != w.kb0 || kk != 0));
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -405,11 +422,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // This CTA's share of a tail tile: fp32 partial sums, row-major 128 x 256.
           float *slot = p.partials + ((int64_t)(w.tile - p.dp_tiles) * p.smax + w.slot) * (BM * BN) +
                         (int64_t)row_in_tile * BN;
+          // slot w.slot of the tail tile's smax (the host sized the buffer for
+          // every tail tile's smax slots)
+          const bool slot_ok = EXL3_RANGE(w.tile - p.dp_tiles, 0, (int64_t)p.tiles_m * p.tiles_n - p.dp_tiles) &&
+                               EXL3_RANGE(w.slot, 0, p.smax);
           const int ncols = second ? BN : 128;
           for (int j = 0; j < ncols; j += 32) {
             float t[32];
             tmem_ld32(tbase + j, t);
-            if (row < p.M) {
+            if (row < p.M && slot_ok) {
               float4 *dst = reinterpret_cast<float4 *>(slot + j);
   #pragma unroll
               for (int a = 0; a < 8; ++a) dst[a] = make_float4(t[4 * a], t[4 * a + 1], t[4 * a + 2], t[4 * a + 3]);
@@ -485,7 +506,8 @@ __global__ void __launch_bounds__(256) prefill_tail_finalize_kernel(const Prefil
   const float *src = p.partials + t * p.smax * (int64_t)(BM * BN) + (int64_t)r * BN + 128 * half + 8 * l16;
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int cnt = (int)(last - first + 1);
-  for (int s = 0; s < cnt; ++s) {  // slot (CTA) order
+  const bool slots_ok = EXL3_RANGE(cnt, 1, p.smax + 1);  // cnt of the tile's smax slots
+  for (int s = 0; s < (slots_ok ? cnt : 0); ++s) {  // slot (CTA) order
     if (half == 0 || second) {
       const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)s * (BM * BN)));
       const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)s * (BM * BN)) + 1);
@@ -514,6 +536,7 @@ __global__ void __launch_bounds__(256) prefill_tail_finalize_kernel(const Prefil
       }
     }
     if (half == 1 && !second) return;
+    if (!EXL3_SPAN(col0, 8, p.nc)) return;
     const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.sv + col0));
     const __half *h = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
@@ -522,6 +545,7 @@ __global__ void __launch_bounds__(256) prefill_tail_finalize_kernel(const Prefil
   } else if (half == 1 && !second) {
     return;
   }
+  if (!EXL3_SPAN(col0, 8, p.nc)) return;
   if (p.y_f32) {
     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + row * p.ldy + col0);
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -563,7 +587,9 @@ bool encode_tensor_map_2d(CUtensorMap *m, CUtensorMapDataType type, const void *
                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t init_prefill_kernels() {
+cudaError_t init_prefill_kernels(int *status) {
+  const cudaError_t eb = EXL3_BIND_BOUNDS_WORD(status);
+  if (eb != cudaSuccess) return eb;
   if (!g_encode) {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -669,5 +695,9 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   prefill_tail_finalize_kernel<<<(unsigned)ceil_div(warps, 8), 256, 0, st>>>(q, kblocks);
   return cudaGetLastError();
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_prefill(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3

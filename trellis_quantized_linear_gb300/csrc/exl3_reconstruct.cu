@@ -47,13 +47,20 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const uint8_t *__restr
     }
     const uint8_t *src = trellis + ((tk * tiles_n + (nb0 + nb) * 8) * kTileBytes) + lane * 8 * BITS;
     uint32_t own[2 * BITS];
-    load_own_words<BITS, false>(src, own);
+    // the slab's 8 tiles: tile row tk of tk_count, tiles [8 (nb0 + nb), +8) of tiles_n
+    if (EXL3_RANGE(tk, 0, tk_count) && EXL3_SPAN((nb0 + nb) * 8, 8, tiles_n)) {
+      load_own_words<BITS, false>(src, own);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * BITS; ++i) own[i] = 0;
+    }
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
     RowWindows<BITS> rw;
     rw.build(own, prev);
     auto pair = [&](uint32_t sa, uint32_t sb) { return decode_pair_sel<true>(sa, sb); };
     const int64_t k0 = tk * 16 + 4 * q;      // first of this lane's 4 rows
     const int64_t j0 = nb * 128 + 16 * g;    // first column of this lane's tile (slice-local)
+    if (!EXL3_SPAN(k0, 4, K) || !EXL3_SPAN(j0, 16, n_cols)) continue;  // the lane's 4 x 16 block of w
     if (LAYOUT == 0) {
       static_for<4>([&](auto R) {
         uint32_t p[8];
@@ -83,8 +90,9 @@ static cudaError_t init_bits() {
   return cudaFuncGetAttributes(&a, reconstruct_kernel<BITS, 1>);
 }
 
-cudaError_t init_reconstruct_kernels() {
-  cudaError_t e;
+cudaError_t init_reconstruct_kernels(int *status) {
+  cudaError_t e = EXL3_BIND_BOUNDS_WORD(status);
+  if (e != cudaSuccess) return e;
   if ((e = init_bits<1>()) != cudaSuccess) return e;
   if ((e = init_bits<7>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
@@ -143,5 +151,9 @@ cudaError_t launch_reconstruct(const uint16_t *trellis, int bits, int64_t K, int
     default: return cudaErrorInvalidValue;
   }
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_reconstruct(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3

@@ -74,6 +74,11 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
   __half *O = reinterpret_cast<__half *>(rr_smem + RR_TN * 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t kb = blockIdx.x / nbc, nb = blockIdx.x % nbc;  // 128-row block, slice-local 128-column block
+  // tiles inside the CTA's shared memory; the block inside K x n_cols and
+  // its sv columns inside the stored width (CTA-uniform)
+  if (!EXL3_SMEM(smem_u32(rr_smem), RR_SMEM) || !EXL3_SPAN(kb * 128, 128, K) || !EXL3_SPAN(nb * 128, 128, n_cols) ||
+      !EXL3_SPAN((nb0 + nb) * 128, 128, tiles_n * 16))
+    return;
 
   // 1. decode slab `warp` of the block
   {
@@ -81,12 +86,18 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
     const int64_t tk = kb * 8 + warp;
     const uint8_t *src = trellis + ((tk * tiles_n + (nb0 + nb) * 8) * (32 * BITS)) + lane * 8 * BITS;
     uint32_t own[2 * BITS];
-    load_own_words<BITS, false>(src, own);
+    if (EXL3_RANGE(warp, 0, 8)) {  // slab kb * 8 + warp of the block's 8
+      load_own_words<BITS, false>(src, own);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * BITS; ++i) own[i] = 0;
+    }
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
     RowWindows<BITS> rw;
     rw.build(own, prev);
     static_for<4>([&](auto R) {
       float *row = T + rr_ix(16 * warp + 4 * q + R.value, 16 * g);  // 16 columns in one half
+      if (!EXL3_SPAN(rr_ix(16 * warp + 4 * q + R.value, 16 * g), 16, RR_TN)) return;
       static_for<8>([&](auto C2) {
         const uint32_t p2 = decode_pair(rw.template state<R.value, 2 * C2.value>(),
                                         rw.template state<R.value, 2 * C2.value + 1>());
@@ -100,14 +111,18 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
 
   const int upper = lane >> 4;
   const int idx = 16 * warp + (lane & 15);  // column (pass 2) / row (pass 3) of this lane pair
-  // 2. column pass along k
+  // 2. column pass along k (the lane's 64 tile entries lie between its first
+  // and last, rr_ix being monotonic in each index)
+  const bool col_ok = EXL3_RANGE(rr_ix(64 * upper, idx), 0, RR_TN) && EXL3_RANGE(rr_ix(64 * upper + 63, idx), 0, RR_TN);
+  const bool row_ok = EXL3_RANGE(rr_ix(idx, 64 * upper), 0, RR_TN) && EXL3_RANGE(rr_ix(idx, 64 * upper + 63), 0, RR_TN);
   {
     float v[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = T[rr_ix(64 * upper + i, idx)];
+    for (int i = 0; i < 64; ++i) v[i] = col_ok ? T[rr_ix(64 * upper + i, idx)] : 0.f;
     wht128_pair(v, upper);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) T[rr_ix(64 * upper + i, idx)] = v[i];
+    for (int i = 0; i < 64; ++i)
+      if (col_ok) T[rr_ix(64 * upper + i, idx)] = v[i];
   }
   __syncthreads();
   // 3. row pass along n, then scale and round
@@ -115,7 +130,7 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
     const float s = __half2float(su[kb * 128 + idx]);
     float v[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(T[rr_ix(idx, 64 * upper + i)], s);
+    for (int i = 0; i < 64; ++i) v[i] = row_ok ? __fmul_rn(T[rr_ix(idx, 64 * upper + i)], s) : 0.f;
     wht128_pair(v, upper);
     const __half *svb = sv + nb0 * 128 + nb * 128 + 64 * upper;
 #pragma unroll
@@ -123,8 +138,9 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
       const float a = __fmul_rn(__fmul_rn(v[i], 0.0078125f), __half2float(svb[i]));
       const float b = __fmul_rn(__fmul_rn(v[i + 1], 0.0078125f), __half2float(svb[i + 1]));
       if (LAYOUT == 0) {
-        *reinterpret_cast<__half2 *>(O + idx * RR_O + 64 * upper + i) = __floats2half2_rn(a, b);
-      } else {
+        if (EXL3_SPAN(idx * RR_O + 64 * upper + i, 2, 128 * RR_O))
+          *reinterpret_cast<__half2 *>(O + idx * RR_O + 64 * upper + i) = __floats2half2_rn(a, b);
+      } else if (EXL3_RANGE((64 * upper + i + 1) * RR_O + idx, 0, 128 * RR_O)) {
         O[(64 * upper + i) * RR_O + idx] = __float2half_rn(a);
         O[(64 * upper + i + 1) * RR_O + idx] = __float2half_rn(b);
       }
@@ -134,6 +150,7 @@ __global__ void __launch_bounds__(256, 2) reconstruct_rotated_kernel(const uint8
   // 4. copy out: 128 rows of 256 bytes, 16 bytes per thread per step
   for (int e = threadIdx.x; e < 128 * 16; e += blockDim.x) {
     const int r = e >> 4, c = (e & 15) * 8;
+    if (!EXL3_SPAN(r * RR_O + c, 8, 128 * RR_O)) continue;
     const uint4 val = *reinterpret_cast<const uint4 *>(O + r * RR_O + c);
     if (LAYOUT == 0)
       *reinterpret_cast<uint4 *>(w + (kb * 128 + r) * n_cols + nb * 128 + c) = val;
@@ -162,8 +179,9 @@ void launch_bits(const uint8_t *t, int64_t tiles_n, int64_t nb0, int64_t nbc, co
 
 }  // namespace
 
-cudaError_t init_reconstruct_rotated_kernels() {
-  cudaError_t e;
+cudaError_t init_reconstruct_rotated_kernels(int *status) {
+  cudaError_t e = EXL3_BIND_BOUNDS_WORD(status);
+  if (e != cudaSuccess) return e;
   if ((e = init_bits<1>()) != cudaSuccess) return e;
   if ((e = init_bits<2>()) != cudaSuccess) return e;
   if ((e = init_bits<3>()) != cudaSuccess) return e;
@@ -197,5 +215,9 @@ cudaError_t launch_reconstruct_rotated(const uint16_t *trellis, int bits, int64_
   }
   return cudaGetLastError();
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_reconstruct_rotated(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3

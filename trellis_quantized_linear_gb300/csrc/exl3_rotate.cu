@@ -33,10 +33,12 @@ __global__ void __launch_bounds__(256) hadamard128_kernel(const __half *x, __hal
     const int64_t off = row * cols + cb * 128 + l16 * 8;
     float v[8];
     if (valid) {
-      uint4 raw = *reinterpret_cast<const uint4 *>(x + off);
+      const uint4 raw = EXL3_SPAN(off, 8, nblk * 128) ? *reinterpret_cast<const uint4 *>(x + off) : uint4{};
       const __half *h = reinterpret_cast<const __half *>(&raw);
       if (pre) {
-        uint4 praw = __ldg(reinterpret_cast<const uint4 *>(pre + cb * 128 + l16 * 8));
+        const uint4 praw = EXL3_SPAN(cb * 128 + l16 * 8, 8, cols)
+                               ? __ldg(reinterpret_cast<const uint4 *>(pre + cb * 128 + l16 * 8))
+                               : uint4{};
         const __half *p = reinterpret_cast<const __half *>(&praw);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = __half2float(h[i]) * __half2float(p[i]);
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(256) hadamard128_kernel(const __half *x, __hal
       __half *o = reinterpret_cast<__half *>(&out);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(v[i] * kInvSqrt128);
-      *reinterpret_cast<uint4 *>(y + off) = out;
+      if (EXL3_SPAN(off, 8, nblk * 128)) *reinterpret_cast<uint4 *>(y + off) = out;
     }
   }
 }
@@ -87,7 +89,8 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(const float *__restric
   float best = -INFINITY;
   int bidx = INT_MAX;
   for (int64_t c = (int64_t)threadIdx.x * 4; c < n; c += (int64_t)blockDim.x * 4) {
-    float4 v = __ldg(reinterpret_cast<const float4 *>(row + c));
+    const float4 v = EXL3_SPAN(c, 4, n) ? __ldg(reinterpret_cast<const float4 *>(row + c))
+                                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -110,13 +113,13 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(const float *__restric
   __shared__ float sb[8];
   __shared__ int si[8];
   const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
+  if ((threadIdx.x & 31) == 0 && EXL3_RANGE(w, 0, 8)) {
     sb[w] = best;
     si[w] = bidx;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
+    for (int i = 1; i < (int)(blockDim.x >> 5) && EXL3_RANGE(i, 0, 8); ++i) {
       if (sb[i] > best || (sb[i] == best && si[i] < bidx)) {
         best = sb[i];
         bidx = si[i];
@@ -175,9 +178,11 @@ cudaError_t launch_silu_mul(const void *gate, const void *up, void *out, int64_t
   return cudaGetLastError();
 }
 
-cudaError_t init_rotate_kernels() {
+cudaError_t init_rotate_kernels(int *status) {
+  cudaError_t e = EXL3_BIND_BOUNDS_WORD(status);
+  if (e != cudaSuccess) return e;
   cudaFuncAttributes a;
-  cudaError_t e = cudaFuncGetAttributes(&a, hadamard128_kernel);
+  e = cudaFuncGetAttributes(&a, hadamard128_kernel);
   if (e != cudaSuccess) return e;
   e = cudaFuncGetAttributes(&a, wait_timeout_selftest_kernel);
   if (e != cudaSuccess) return e;
@@ -206,5 +211,9 @@ cudaError_t launch_argmax(const float *logits, int64_t M, int64_t n, int32_t *ar
   argmax_rows_kernel<<<(unsigned)M, 256, 0, st>>>(logits, n, argmax);
   return cudaGetLastError();
 }
+
+#if EXL3_DEBUG_BOUNDS
+cudaError_t bounds_probe_rotate(cudaStream_t st) { return launch_bounds_probe(st); }
+#endif
 
 }  // namespace exl3
