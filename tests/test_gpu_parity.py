@@ -217,6 +217,47 @@ def test_prefill_chunks_past_32768_columns(oracle):
         assert rel_err(y, ref) <= TOL
 
 
+def test_empty_inputs_are_no_ops():
+    # M = 0 rows (and zero rows / columns for the building blocks) is a valid
+    # call on every entry point: EXL3_OK, nothing written, no device error.
+    torch = torch_mod()
+    K, N, bits = 256, 384, 4
+    m = synthetic.make_matrix(K, N, bits, seed=21)
+    L = Layer(m)
+    x = torch.ones((1, K), dtype=torch.float16, device="cuda")  # valid pointer; no row is read
+    for thr in (DECODE, PREFILL, 1000):
+        ws = L.workspace(1, thr)
+        y = torch.full((1, N), 7.0, dtype=torch.float32, device="cuda")
+        am = torch.full((4,), -5, dtype=torch.int32, device="cuda")
+        tql.exl3_linear(x, 0, K, L.trellis, bits, N, N, L.su, L.sv, y, tql.EXL3_F32, thr, ws)
+        tql.exl3_logits_masked(x, 0, K, L.trellis, bits, N, N, N - 3, L.su, L.sv, y, am, thr, ws)
+        torch.cuda.synchronize()
+        assert bool(torch.all(y == 7.0)) and bool(torch.all(am == -5))
+    y16 = torch.full((1, N), 3.0, dtype=torch.float16, device="cuda")
+    tql.exl3_linear_decode_noalloc(x, 0, K, L.trellis, bits, N, N, L.su, L.sv, y16, tql.EXL3_F16)
+    xr = torch.full((1, K), 3.0, dtype=torch.float16, device="cuda")
+    tql.exl3_hadamard128(x, xr, L.su, rows=0, cols=K)
+    w = torch.full((K, 128), 3.0, dtype=torch.float16, device="cuda")
+    tql.exl3_reconstruct(L.trellis, bits, K, N, 128, 0, w, tql.EXL3_LAYOUT_KN)
+    tql.exl3_reconstruct_rotated(L.trellis, bits, K, N, 128, 0, L.su, L.sv, w, tql.EXL3_LAYOUT_KN)
+    torch.cuda.synchronize()
+    assert bool(torch.all(y16 == 3.0)) and bool(torch.all(xr == 3.0)) and bool(torch.all(w == 3.0))
+    assert tql.exl3_get_device_status() == 0
+
+
+# The largest K the ABI accepts (131072 = 2^17): 8192 k slabs per n-block on
+# the decode path, 2048 k steps on the tensor-core decode path, a 2048-block
+# K loop (stream-K tail split) on the prefill path.
+@pytest.mark.parametrize("M,thr", [(1, DECODE), (16, DECODE), (40, DECODE), (200, PREFILL)])
+def test_maximum_k(oracle, M, thr):
+    K, N, bits = 131072, 256, 2
+    m = synthetic.make_matrix(K, N, bits, seed=31)
+    x = synthetic.make_activations(M, K, seed=31)
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    y = Layer(m).linear(to_dev(x), thr).cpu().numpy()
+    assert rel_err(y, ref) <= TOL
+
+
 def test_runtime_dispatch_uses_threshold(oracle):
     K, N, bits = 256, 256, 4
     m = synthetic.make_matrix(K, N, bits, seed=5)
