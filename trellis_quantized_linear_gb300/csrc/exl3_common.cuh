@@ -90,6 +90,33 @@ struct RowWindows {
     }
   }
 
+  // The same state with at most one integer-pipe instruction: the view
+  // X << k, k = o mod 8, is a multiply by mk[k] = 2^k on the FMA pipe (mk
+  // opaque to the compiler, so the multiply is not turned into a shift).
+  // The window then starts at bit 16 or 24 of the view: one shift or one
+  // byte permute. Two windows of one X word with the same k share the view.
+  template <int R, int C>
+  __device__ __forceinline__ uint32_t state_fma(const uint32_t (&mk)[8]) const {
+    constexpr int s = R * BITS * 16 + (C + 1) * BITS;  // window start, in seq bits
+    constexpr int j = s >> 4;
+    constexpr int o = s & 15;
+    constexpr int k = o & 7;
+    static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
+    static_assert(o == 0 ? (j >= 1 && j <= kWords) : (j >= 0 && j < kWords), "window outside X");
+    if constexpr (o == 0) {
+      return X[j - 1] & 0xFFFFu;  // seq[j]
+    } else if constexpr (k == 0) {
+      return __byte_perm(X[j], 0u, 0x4421);  // o == 8
+    } else {
+      const uint32_t v = X[j] * mk[k];  // window at bits 31-(o-k) .. 16-(o-k), o - k in {0, 8}
+      if constexpr (o == k) {
+        return v >> 16;
+      } else {
+        return __byte_perm(v, 0u, 0x4421);
+      }
+    }
+  }
+
   // 16-bit state of weight c (0..15) of thread row r (0..3).
   template <int R, int C>
   __device__ __forceinline__ uint32_t state() const {
@@ -141,43 +168,6 @@ __device__ __forceinline__ uint32_t decode_dup(uint32_t state) {
   const __half2 r = __hadd2(__low2half2(h), __high2half2(h));
   return *reinterpret_cast<const uint32_t *>(&r);
 }
-
-// Window states of a lane's four rows; for BITS = 4 a nibble-shifted copy
-// of the words (a funnel shift per word) makes every state one instruction.
-template <int BITS>
-struct Windows {
-  RowWindows<BITS> rw;
-  uint32_t X4[4 * BITS];
-  __device__ __forceinline__ void build(const uint32_t (&own)[2 * BITS], uint32_t prev) {
-    rw.build(own, prev);
-    if constexpr (BITS == 4) {
-#pragma unroll
-      for (int j = 0; j + 1 < 4 * BITS; ++j) X4[j] = __funnelshift_l(rw.X[j + 1], rw.X[j], 4);
-      X4[4 * BITS - 1] = rw.X[4 * BITS - 1] << 4;
-    }
-  }
-  template <int R, int C>
-  __device__ __forceinline__ uint32_t state() const {
-    if constexpr (BITS == 4) {
-      constexpr int s = R * 64 + (C + 1) * 4;
-      constexpr int j = s >> 4;
-      constexpr int o = s & 15;
-      static_assert(R >= 0 && R < 4 && C >= 0 && C < 16, "window index out of range");
-      static_assert(o == 0 ? (j >= 1 && j <= 4 * BITS) : (j >= 0 && j < 4 * BITS), "window outside X / X4");
-      if constexpr (o == 0) {
-        return rw.X[j - 1] & 0xFFFFu;  // seq[j], the low half of X[j-1]
-      } else if constexpr (o == 8) {
-        return __byte_perm(rw.X[j], 0u, 0x4421);
-      } else if constexpr (o == 4) {
-        return X4[j] >> 16;
-      } else {
-        return __byte_perm(X4[j], 0u, 0x4421);
-      }
-    } else {
-      return rw.template state<R, C>();
-    }
-  }
-};
 
 // The 16 window states of one tile row for BITS = 4. A and B hold the row's
 // own words w0..w3 as two little-endian uint32 (w1 << 16 | w0, w3 << 16 | w2);

@@ -61,9 +61,12 @@ template <int BITS, int MT>
 struct DecodeCfg {
   static constexpr int kWarps = dec_warps<MT>();
   static constexpr int kSeg = 256 * BITS;                    // trellis bytes per slab
-  static constexpr int kChunk = BITS <= 4 ? 4 : 2;           // slabs per copy
-  static constexpr int kStages = MT == 1 ? 2 : 3;            // ring stages (chunks) per warp
+  // slabs per copy: 4, or 3 where two stages of 4 would not fit (8 bits)
+  static constexpr int kChunk = 2 * kWarps * 4 * (kSeg + kXFrag) <= 226 * 1024 ? 4 : 3;
   static constexpr int kStage = kChunk * (kSeg + kXFrag);    // trellis box, then the chunk's x'
+  // ring stages (chunks) per warp: 2 for <= 8 rows; 3 for 9..16 rows where
+  // they fit
+  static constexpr int kStages = (MT == 2 && 3 * kWarps * kStage <= 226 * 1024) ? 3 : 2;
   static constexpr int kWarpRing = kStages * kStage;
   static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8;
   static_assert(kSmem <= 227 * 1024, "decode ring exceeds shared memory");
@@ -78,6 +81,7 @@ struct DecodeParams {
   int64_t n_gemm, n_valid;
   int TS, P, KT, rows, y_f32, smax;
   uint32_t m16;  // 16, opaque to the compiler (a multiply by it stays on the FMA pipe)
+  uint32_t mk[8];  // mk[k] = 2^k, opaque likewise (window views for widths other than 4)
 };
 
 __device__ __forceinline__ void tma_load_2d_u64(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
@@ -255,7 +259,7 @@ __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol
 // The lane's 64 states of one slab: st[r][c] = tile row 4q + r, column c.
 template <int BITS>
 __device__ __forceinline__ void slab_states(const uint32_t (&own)[2 * BITS], uint32_t prev, uint32_t m16,
-                                            uint32_t (&st)[4][16]) {
+                                            const uint32_t (&mk)[8], uint32_t (&st)[4][16]) {
   if constexpr (BITS == 4) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) row4_states(own[2 * r], own[2 * r + 1], r == 0 ? prev : own[2 * r - 1], m16, st[r]);
@@ -263,7 +267,7 @@ __device__ __forceinline__ void slab_states(const uint32_t (&own)[2 * BITS], uin
     RowWindows<BITS> rw;
     rw.build(own, prev);
     static_for<4>([&](auto R) {
-      static_for<16>([&](auto C) { st[R.value][C.value] = rw.template state<R.value, C.value>(); });
+      static_for<16>([&](auto C) { st[R.value][C.value] = rw.template state_fma<R.value, C.value>(mk); });
     });
   }
 }
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
                           : uint4{};
     const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
     uint32_t st[4][16];
-    slab_states<BITS>(own, prev, p.m16, st);
+    slab_states<BITS>(own, prev, p.m16, p.mk, st);
     if constexpr (MT == 1) {
       // B registers {x'[row], 0} for tile rows 4q .. 4q+3 of token g
       static_for<8>([&](auto J) {
@@ -828,6 +832,7 @@ cudaError_t launch_decode_gemm(const DecodeLaunch &L, cudaStream_t st) {
   dp.smax = (int)L.plan.smax[MT - 1];
   dp.rows = L.rows;
   dp.m16 = 16u;
+  for (int k = 0; k < 8; ++k) dp.mk[k] = 1u << k;
   dp.y_f32 = L.y_f32;
   const int64_t grid = L.plan.grid[MT - 1];
   const int64_t tiles_n = L.n_stored / 16;

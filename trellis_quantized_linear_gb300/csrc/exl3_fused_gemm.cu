@@ -426,10 +426,12 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 #pragma unroll
         for (int r = 0; r < 4; ++r) row4_states(own[2 * r], own[2 * r + 1], r == 0 ? prev : own[2 * r - 1], p.m16, st[r]);
       } else {
-        Windows<BITS> win;
-        win.build(own, prev);
+        RowWindows<BITS> rw;
+        rw.build(own, prev);
         static_for<4>([&](auto R) {
-          static_for<16>([&](auto C) { st[R.value][C.value] = win.template state<R.value, C.value>(); });
+          // plain extraction: the window views' multiplies measured mixed here (the
+          // decoders load the FMA pipe too), -4 % to +4.5 % over bits 1..8
+          static_for<16>([&](auto C) { st[R.value][C.value] = rw.template state<R.value, C.value>(); });
         });
       }
       if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) {
