@@ -468,8 +468,12 @@ __global__ void __launch_bounds__(DecodeCfg<BITS, MT>::kWarps * 32, 1)
     }
     const uint8_t *stage = ring + s * Cfg::kStage;
     const uint8_t *xst = stage + CHK * Cfg::kSeg;
-#pragma unroll 2
-    for (int i = 0; i < len; ++i) slab(stage + i * Cfg::kSeg, xst + i * kXFrag);
+    if (len == CHK) {  // a full chunk: straight-line slabs the scheduler can interleave
+      static_for<CHK>([&](auto I) { slab(stage + I.value * Cfg::kSeg, xst + I.value * kXFrag); });
+    } else {
+#pragma unroll 1
+      for (int i = 0; i < len; ++i) slab(stage + i * Cfg::kSeg, xst + i * kXFrag);
+    }
     // a chunk lies inside one n-block, so only its end can end this warp's part of it
     tk += len;
     z += len;
