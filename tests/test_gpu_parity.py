@@ -245,6 +245,20 @@ def test_empty_inputs_are_no_ops():
     assert tql.exl3_get_device_status() == 0
 
 
+# The smallest shapes the ABI accepts: one 128-row k block and one 128-column
+# n block (8 k slabs for the decode path, a half-width tile on the prefill
+# path), on every path.
+@pytest.mark.parametrize("bits", [1, 4, 8])
+@pytest.mark.parametrize("M,thr", [(1, DECODE), (16, DECODE), (17, DECODE), (200, PREFILL)])
+def test_smallest_shapes(oracle, bits, M, thr):
+    K, N = 128, 128
+    m = synthetic.make_matrix(K, N, bits, seed=41 + bits)
+    x = synthetic.make_activations(M, K, seed=41 + M)
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    y = Layer(m).linear(to_dev(x), thr).cpu().numpy()
+    assert rel_err(y, ref) <= TOL
+
+
 # The largest K the ABI accepts (131072 = 2^17): 8192 k slabs per n-block on
 # the decode path, 2048 k steps on the tensor-core decode path, a 2048-block
 # K loop (stream-K tail split) on the prefill path.
