@@ -64,9 +64,9 @@ struct DecodeCfg {
   // slabs per copy: 4, or 3 where two stages of 4 would not fit (8 bits)
   static constexpr int kChunk = 2 * kWarps * 4 * (kSeg + kXFrag) <= 226 * 1024 ? 4 : 3;
   static constexpr int kStage = kChunk * (kSeg + kXFrag);    // trellis box, then the chunk's x'
-  // ring stages (chunks) per warp: 2 for <= 8 rows; 3 for 9..16 rows where
-  // they fit
-  static constexpr int kStages = (MT == 2 && 3 * kWarps * kStage <= 226 * 1024) ? 3 : 2;
+  // ring stages (chunks) per warp (with full chunks run as straight-line
+  // slabs, a third stage measured slower for 1..8 rows and for 9..16 rows)
+  static constexpr int kStages = 2;
   static constexpr int kWarpRing = kStages * kStage;
   static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8;
   static_assert(kSmem <= 227 * 1024, "decode ring exceeds shared memory");
