@@ -789,9 +789,10 @@ cudaError_t launch_decode_finalize(const float *partials, int64_t smax, int64_t 
                                    int units_per_block, int all_blocks, cudaStream_t st) {
   if (!all_blocks) {
     const int64_t warps = (n_gemm / 128) * rows;
-    // One warp per CTA for 1-2 rows spreads the slot loads over more SMs
-    // (0.35 us less at 1 row, 0.1 us at 2; 4 rows measured 0.1 us slower).
-    const unsigned wpc = rows <= 2 ? 1u : 8u;
+    // One warp per CTA for 1-4 rows spreads the slot loads over more SMs
+    // (0.35 us less at 1 row, 0.1 us at 2, 0.25 us at 4; 8 rows measured
+    // 0.1 us slower).
+    const unsigned wpc = rows <= 4 ? 1u : 8u;
     return launch_dependent(decode_finalize_kernel, (unsigned)ceil_div(warps, (int64_t)wpc), 32u * wpc, (size_t)0, st,
                             partials, smax, slot_elems, static_cast<const __half *>(sv), y, y_f32, n_gemm, n_valid,
                             rows, P, TS, units_per_block, all_blocks);
