@@ -63,8 +63,9 @@ struct FusedCfg {
   static constexpr int kSeg = 256 * BITS;
   // Trellis bytes each decoder warp keeps in flight (at least two slabs):
   // 16 warps x 2 KB per SM covers the HBM latency at the rate the decoders
-  // consume.
-  static constexpr int kRingBytes = 2048;
+  // consume; at 4 bits three slabs measured 0.1-0.9 us faster at 32..256
+  // rows (4 KB: slower below 128 rows).
+  static constexpr int kRingBytes = BITS == 4 ? 3072 : 2048;
   static constexpr int kRD = kRingBytes / kSeg < 2 ? 2 : kRingBytes / kSeg;
   static constexpr int kBudget = 227 * 1024 - 2048 - 2048;
   static constexpr int kRest = kBudget - F_DEC_WARPS * kRD * kSeg;
