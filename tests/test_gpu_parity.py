@@ -190,6 +190,20 @@ def test_prefill_stream_k_tail(oracle, K, N, n_dec, M):
     assert np.array_equal(am.cpu().numpy(), np.argmax(lg, axis=1))
 
 
+@pytest.mark.parametrize("M,bits", [(300, 4), (1100, 2), (512, 5)])
+def test_prefill_pair_tiles(oracle, M, bits):
+    """Prefill-shaped calls that run as CTA-pair tiles (256 x 256, two SMs per
+    tile): an odd number of 128-row tiles (M = 300, 1100), whose last pair
+    has no second row tile, and an even one; 20 tile columns, so no split
+    tail. Every output checked."""
+    K, N = 512, 5120
+    m = synthetic.make_matrix(K, N, bits, seed=M + bits)
+    x = synthetic.make_activations(M, K, seed=M)
+    y = Layer(m).linear(to_dev(x), PREFILL).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
+
+
 def test_tiny_workload_both_paths_and_fp16_rounding(oracle):
     t = synthetic.TINY
     m = synthetic.make_matrix(t["K"], t["N"], t["bits"], seed=t["seed"])

@@ -58,6 +58,7 @@ struct PrefillParams {
   // several CTAs is accumulated in fp32 partial slots (128 x 256, in CTA
   // order) that prefill_tail_finalize_kernel reduces.
   int G, full_waves, dp_tiles, Gsk, smax;
+  int pair_cols;  // CTA-pair launch: tile columns 0 .. pair_cols-1, every tile row
   int64_t U;
   float *partials;
 };
@@ -484,6 +485,225 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if constexpr (SK) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// CTA-pair form of the whole-tile launch. A cluster of two CTAs (two SMs)
+// computes one 256 x 256 output tile with tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16): the even CTA (rank 0) stages x' rows 0-127 of the tile and
+// W^T rows (output columns) 0-127, the odd CTA rows 128-255 of each, and the
+// even CTA's thread issues the MMA for both. Each SM thus stages 32 KB per
+// 64-deep k block (16 KB of A, 16 KB of B) instead of the 48 KB of a
+// one-SM 128 x 256 tile, for the same tensor work per SM. Each CTA's TMEM
+// holds its 128 rows x 256 columns (double-buffered, 512 columns), and its
+// four epilogue warps run the same fused had_r_128 / sv / mask epilogue.
+//
+// Barriers (same offsets in both CTAs):
+//   full[s]   rank 0's counts both CTAs' TMA bytes of stage s (the odd CTA's
+//             loads complete on it through its cluster address);
+//   empty[s]  each CTA's, completed by the pair MMA's commit (multicast);
+//   tfull[a]  each CTA's, accumulator a ready (commit, multicast);
+//   tempty[a] rank 0's, 8 arrivals: the four epilogue warps of both CTAs;
+//   done      rank 0's, every pair MMA finished.
+constexpr int P_STAGES = 6;
+constexpr int PA_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of x'
+constexpr int PB_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of W^T
+constexpr int P_RING_BYTES = P_STAGES * (PA_BYTES + PB_BYTES);
+constexpr int P_NBARS = 2 * P_STAGES + 5;
+constexpr int P_SMEM_BYTES = 1024 + P_RING_BYTES + 256;
+static_assert(P_NBARS * 8 + 4 <= 256, "pair barrier area");
+constexpr uint32_t kIdescPair = f16_idesc(256, 256);
+
+// Pair tile t: rows 256 (t % tiles_mp) .., columns 256 (t / tiles_mp) ..,
+// for the first pair_cols tile columns.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_RING_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P_NBARS);
+  const uint32_t smem_s = smem_u32(smem);
+  auto a_s = [&](int s) { return smem_s + (uint32_t)(s * PA_BYTES); };
+  auto b_s = [&](int s) { return smem_s + (uint32_t)(P_STAGES * PA_BYTES + s * PB_BYTES); };
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[P_STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * P_STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * P_STAGES + 2 + a]); };
+  const uint32_t done_bar = smem_u32(&bars[2 * P_STAGES + 4]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  const int kblocks = p.K / BK;
+  const int tiles_mp = (p.tiles_m + 1) >> 1;
+  const int ptiles = tiles_mp * p.pair_cols;
+  // Ring, barriers and TMEM slot inside the CTA's shared memory. The same
+  // in both CTAs (same kernel, same size), so both leave here or neither.
+  if (!EXL3_SMEM(smem_s, P_RING_BYTES + P_NBARS * 8 + 4)) return;
+  // This CTA's boxes of pair tile (tmp, tn) at k block kb: fp16 column 64 kb
+  // (128 bytes: the 16-byte rule); 128 x' rows inside the rotated rows, W^T
+  // rows 256 tn + 128 rank inside the chunk.
+  auto box_ok = [&](int tmp, int tn, int kb) {
+    return EXL3_RANGE(tmp, 0, tiles_mp) && EXL3_RANGE(tn, 0, p.pair_cols) && EXL3_RANGE(kb, 0, kblocks) &&
+           EXL3_ALIGNED(kb * BK * 2, 16);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {  // one warp of each CTA of the pair allocates together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // both CTAs' barriers initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int t = pair; t < ptiles && ok; t += npairs) {
+      const int tmp = t % tiles_mp, tn = t / tiles_mp;
+      // With an odd number of 128-row tiles the last pair's odd CTA re-reads
+      // the last real row tile (its rows are past M and never stored).
+      const int arow = min(tmp * 256 + (int)rank * 128, (p.tiles_m - 1) * 128);
+      const int brow = tn * 256 + (int)rank * 128;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, p.status, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (PA_BYTES + PB_BYTES));
+        if (box_ok(tmp, tn, kb)) {
+          const uint32_t fb = map_to_rank(full_bar(stage), 0);
+          tma_load_2d_pair(a_s(stage), &tmA, fb, kb * BK, arow);
+          tma_load_2d_pair(b_s(stage), &tmB, fb, kb * BK, brow);
+        }
+        ++issued;
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Rank 0's full barriers count both CTAs' bytes: once each stage's last
+    // use has completed there, no copy of either CTA is in flight (the final
+    // cluster barrier keeps the odd CTA until then).
+    if (rank == 0)
+      for (int s = 0; s < P_STAGES; ++s) {
+        const int64_t uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+        if (uses > 0) mbar_wait_cluster(full_bar(s), (uint32_t)((uses - 1) & 1), nullptr, 200000000ull);
+      }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (even CTA) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int local = 0;
+    for (int t = pair; t < ptiles && ok; t += npairs, ++local) {
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait_cluster(tempty_bar(acc), (use & 1u) ^ 1u, p.status, kWaitLimitNs)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_cluster(full_bar(stage), phase, p.status, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(a_s(stage));
+        const uint64_t bd = sw128_desc(b_s(stage));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // +32 bytes per 16-element K step inside the 128-byte swizzle atom
+          if (EXL3_RANGE(acc, 0, 2))  // 256 columns of the 512 allocated
+            tc_mma_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdescPair, (kb | kk) != 0);
+        }
+        tc_commit_pair(empty_bar(stage), 3);
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit_pair(tfull_bar(acc), 3);
+    }
+    // All issued MMAs (which write both CTAs' TMEM) finish before the final
+    // cluster barrier, after which both CTAs release their TMEM.
+    tc_commit_pair(done_bar, 1);
+    mbar_wait_cluster(done_bar, 0, nullptr, 200000000ull);
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int lg = warp & 3;  // TMEM lane group this warp may access
+    const int row_in_tile = (int)rank * 128 + lg * 32 + lane;
+    int local = 0;
+    for (int t = pair; t < ptiles; t += npairs, ++local) {
+      const int tmp = t % tiles_mp, tn = t / tiles_mp;
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait_cluster(tfull_bar(acc), use & 1u, p.status, kWaitLimitNs)) break;
+      tc_fence_after();
+      const int64_t row = (int64_t)tmp * 256 + row_in_tile;
+      const uint32_t tbase = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t te = map_to_rank(tempty_bar(acc), 0);
+      const int c0 = tn * BN;
+      const bool second = c0 + 128 < p.nc;
+      float v[128];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float tt[32];
+        tmem_ld32(tbase + 32 * j, tt);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 * j + i] = tt[i];
+      }
+      if (!second) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(te);
+      }
+      epilogue_block(v, p, row, c0);
+      if (second) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float tt[32];
+          tmem_ld32(tbase + 128 + 32 * j, tt);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * j + i] = tt[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(te);
+        epilogue_block(v, p, row, c0 + 128);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // no remote arrival or copy of either CTA is pending
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // Reduces the partial slots of every tail tile shared by several CTAs, in
 // CTA order, then applies the epilogue (had_r_128 per 128-column block, sv,
 // mask) and stores y. One warp per (tail tile, row); lane l holds the eight
@@ -603,6 +823,8 @@ cudaError_t init_prefill_kernels(int *status) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(prefill_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   cudaFuncAttributes a;
   return cudaFuncGetAttributes(&a, prefill_tail_finalize_kernel);
 }
@@ -646,23 +868,45 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   // (re-read from HBM when the chunk exceeds L2) cost more than the idle
   // SMs of the last wave (measured on the 4-bit MLP geometries).
   const bool split_tail = p.U > 0 && 2 * tail <= p.G && (2 * ntiles <= p.G || kblocks >= 128);
-  if (p.U > 0 && !split_tail) {
+  p.pair_cols = 0;
+  const int G2 = L.num_sms / 2;
+  if (p.tiles_m >= 2 && G2 >= 1) {
+    // CTA pairs over 256 x 256 tiles: the same rule in pair units. A split
+    // tail keeps whole tile columns in the pair launch (those the full pair
+    // waves cover) and spreads the remaining columns' 128-row tiles over
+    // all CTAs as below; a problem whose full pair waves cover no whole
+    // column keeps the one-SM schedule.
+    const int tiles_mp = (p.tiles_m + 1) / 2;
+    const int64_t P = (int64_t)tiles_mp * p.tiles_n, tailp = P % G2;
+    const bool split = tailp > 0 && 2 * tailp <= G2 && (2 * P <= G2 || kblocks >= 128);
+    p.pair_cols = split ? (int)((P / G2) * G2 / tiles_mp) : p.tiles_n;
+  }
+  if (p.pair_cols > 0) {
+    p.full_waves = 0;
+    p.dp_tiles = p.pair_cols * p.tiles_m;
+    p.U = (int64_t)(ntiles - p.dp_tiles) * kblocks;
+  } else if (p.U > 0 && !split_tail) {
     p.full_waves += 1;
     p.dp_tiles = ntiles;
     p.U = 0;
   }
+  const int64_t tail_tiles = ntiles - p.dp_tiles;
   if (p.U > 0) {
     int64_t gsk = p.U / 4;
     if (gsk < 1) gsk = 1;
     if (gsk > p.G) gsk = p.G;
     int64_t smax = 1;
-    for (int64_t t = 0; t < tail; ++t) {
+    for (int64_t t = 0; t < tail_tiles; ++t) {
       const int64_t c = (((t + 1) * kblocks) * gsk - 1) / p.U - (((t * kblocks + 1) * gsk - 1) / p.U) + 1;
       if (c > smax) smax = c;
     }
-    if (L.partials != nullptr && (size_t)(tail * smax) * BM * BN * 4 <= L.partials_bytes) {
+    if (L.partials != nullptr && (size_t)(tail_tiles * smax) * BM * BN * 4 <= L.partials_bytes) {
       p.Gsk = (int)gsk;
       p.smax = (int)smax;
+    } else if (p.pair_cols > 0) {  // no room for partial slots: every column in pair tiles
+      p.pair_cols = p.tiles_n;
+      p.dp_tiles = ntiles;
+      p.U = 0;
     } else {  // no room for partial slots: the tail runs as one more wave of whole tiles
       p.full_waves += 1;
       p.dp_tiles = ntiles;
@@ -671,7 +915,15 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   }
   // Whole tiles first (data-parallel waves), then, when the tail is split, a
   // second launch that spreads the tail's k blocks over Gsk CTAs.
-  if (p.dp_tiles > 0) {
+  if (p.pair_cols > 0) {
+    alignas(64) CUtensorMap mbp;  // W^T boxes of 128 rows: each CTA stages half of a tile's columns
+    if (!make_map(&mbp, L.wt, L.chunk_rows, L.K, 128)) return cudaErrorInvalidValue;
+    const int64_t ptiles = (int64_t)((p.tiles_m + 1) / 2) * p.pair_cols;
+    const int pairs = (int)(ptiles < G2 ? ptiles : G2);
+    prefill_pair_kernel<<<2 * pairs, NUM_THREADS, P_SMEM_BYTES, st>>>(ma, mbp, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (p.dp_tiles > 0) {
     prefill_gemm_kernel<false><<<p.dp_tiles < p.G ? p.dp_tiles : p.G, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -691,7 +943,7 @@ cudaError_t launch_prefill_gemm(const PrefillLaunch &L, cudaStream_t st) {
   cfg.numAttrs = p.dp_tiles > 0 ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<true>, ma, mb, q);
   if (e != cudaSuccess) return e;
-  const int64_t warps = tail * BM;
+  const int64_t warps = tail_tiles * BM;
   prefill_tail_finalize_kernel<<<(unsigned)ceil_div(warps, 8), 256, 0, st>>>(q, kblocks);
   return cudaGetLastError();
 }

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "exl3_common.cuh"
+
 namespace exl3 {
 
 // Shared-memory matrix descriptor for a K-major operand with 128-byte
@@ -70,6 +72,94 @@ __device__ __forceinline__ uint64_t noswizzle_desc(uint32_t saddr, uint32_t lbo,
 // Instruction descriptor, kind::f16 with fp16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair (cta_group::2) forms: a cluster of two CTAs on two SMs shares one
+// MMA. The even CTA of the pair (cluster rank 0) issues it; the operands are
+// read from the same shared-memory offsets in both CTAs and each CTA's TMEM
+// holds its half of the accumulator rows.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`
+// (a shared::cluster address).
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Every thread of both CTAs; orders what each did before against what the
+// other does after (barrier initialisation, the end of all remote arrivals).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA of the pair (`bar` is a
+// shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Arrives once on the mbarrier at offset `bar` of every CTA in `mask` when
+// the pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(bar),
+               "h"(mask)
+               : "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its
+// shared::cluster address, possibly in the peer CTA.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait on a local mbarrier with acquire at cluster scope (for
+// barriers that the peer CTA's threads or the pair MMA complete).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status,
+                                                  unsigned long long limit_ns) {
+  auto try_wait = [&](uint32_t hint) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint)
+        : "memory");
+    return ok != 0;
+  };
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (try_wait(20000u)) return true;
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+      if (status) report_timeout(status);
+      return false;
+    }
+  }
 }
 
 }  // namespace exl3
