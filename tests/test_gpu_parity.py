@@ -190,13 +190,13 @@ def test_prefill_stream_k_tail(oracle, K, N, n_dec, M):
     assert np.array_equal(am.cpu().numpy(), np.argmax(lg, axis=1))
 
 
-@pytest.mark.parametrize("M,bits", [(300, 4), (1100, 2), (512, 5)])
-def test_prefill_pair_tiles(oracle, M, bits):
+@pytest.mark.parametrize("M,bits,N", [(300, 4, 5120), (1100, 2, 5120), (512, 5, 5120), (1100, 3, 5248)])
+def test_prefill_pair_tiles(oracle, M, bits, N):
     """Prefill-shaped calls that run as CTA-pair tiles (256 x 256, two SMs per
     tile): an odd number of 128-row tiles (M = 300, 1100), whose last pair
-    has no second row tile, and an even one; 20 tile columns, so no split
-    tail. Every output checked."""
-    K, N = 512, 5120
+    has no second row tile, and an even one; no split tail; N = 5248 ends in
+    a tile column only 128 wide. Every output checked."""
+    K = 512
     m = synthetic.make_matrix(K, N, bits, seed=M + bits)
     x = synthetic.make_activations(M, K, seed=M)
     y = Layer(m).linear(to_dev(x), PREFILL).cpu().numpy()
