@@ -46,7 +46,7 @@ torch.cuda.set_device(0)
 tql.exl3_init(0)
 assert tql.exl3_bounds_checked()
 rep, tot = tql.exl3_selftest_bounds()
-assert (rep, tot) == (6, 6), (rep, tot)
+assert (rep, tot) == (7, 7), (rep, tot)
 assert tql.exl3_get_device_status() == 0
 print("bounds selftest ok")
 """

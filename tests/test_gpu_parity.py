@@ -171,7 +171,7 @@ def test_linear_prefill_path(oracle, K, N, bits, M):
 
 
 @pytest.mark.parametrize("K,N,n_dec,M", [(2048, 384, 300, 6), (1024, 640, 640, 130), (4096, 256, 256, 1),
-                                         (512, 33152, 33000, 3)])
+                                         (512, 33152, 33000, 520)])
 def test_prefill_stream_k_tail(oracle, K, N, n_dec, M):
     """Prefill-shaped calls whose tiles do not fill a wave: the tail tiles'
     k blocks are spread over all CTAs and reduced from fp32 partial slots,
@@ -204,6 +204,40 @@ def test_prefill_pair_tiles(oracle, M, bits, N):
     assert rel_err(y, ref) <= TOL
 
 
+# The fused prefill kernel (CTA pairs, 512-row x 256-column tiles, the
+# trellis decoded into the MMA operand) serves prefill-shaped calls of at most
+# 512 rows on layers with at least 46 column blocks of 256 (152 SMs).
+@pytest.mark.parametrize("bits,M,N", [(b, 300, 12288) for b in range(1, 9)] +
+                         [(4, 1, 12288), (4, 200, 12288), (4, 512, 12288), (3, 300, 12416), (5, 512, 12416)])
+def test_fused_prefill_path(oracle, bits, M, N):
+    """Every bit width; one and two 256-row sub-blocks (M <= 256, > 256),
+    a partial second sub-block (M = 300), a full tile (M = 512); N = 12416
+    ends in a 128-wide column block, whose odd CTA decodes a block it never
+    stores. Every output against the oracle, fp32 and fp16 (RNE of fp32)."""
+    K = 512
+    m = synthetic.make_matrix(K, N, bits, seed=N + bits + M)
+    x = synthetic.make_activations(M, K, seed=M + bits)
+    L = Layer(m)
+    xd = to_dev(x)
+    y32 = L.linear(xd, PREFILL, tql.EXL3_F32).cpu().numpy()
+    y16 = L.linear(xd, PREFILL, tql.EXL3_F16).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y32, ref) <= TOL
+    assert np.array_equal(y16.view(np.uint16), y32.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [300, 512])
+def test_fused_prefill_full_gate_geometry(oracle, M):
+    """The fused prefill on the whole gate_proj geometry (K=5120, N=17408):
+    68 column blocks on 76 CTA pairs, every output column of every row."""
+    K, N, bits = 5120, 17408, 4
+    m = synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED)
+    x = synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED)
+    y = Layer(m).linear(to_dev(x), 128).cpu().numpy()
+    ref = oracle.linear(x, m.trellis, bits, K, N, m.su, m.sv)
+    assert rel_err(y, ref) <= TOL
+
+
 def test_tiny_workload_both_paths_and_fp16_rounding(oracle):
     t = synthetic.TINY
     m = synthetic.make_matrix(t["K"], t["N"], t["bits"], seed=t["seed"])
@@ -219,8 +253,9 @@ def test_tiny_workload_both_paths_and_fp16_rounding(oracle):
 
 
 def test_prefill_chunks_past_32768_columns(oracle):
-    # n_gemm = 32768 + 384: two reconstruct chunks, the second narrower than a GEMM tile
-    K, N, bits, M = 128, 33152, 4, 5
+    # n_gemm = 32768 + 384: two reconstruct chunks, the second narrower than a
+    # GEMM tile (M > 512, so the prefill side is reconstruct + GEMM)
+    K, N, bits, M = 128, 33152, 4, 520
     m = synthetic.make_matrix(K, N, bits, seed=9)
     x = synthetic.make_activations(M, K, seed=9)
     L = Layer(m)
@@ -382,7 +417,7 @@ def test_prefill_full_size_sampled_rows(oracle, geom):
     assert rel_err(got, ref) <= TOL
 
 
-@pytest.mark.parametrize("M,thr,n_rows", [(1, 128, 1), (16, 128, 16), (64, 128, 16), (2048, 128, 64)])
+@pytest.mark.parametrize("M,thr,n_rows", [(1, 128, 1), (16, 128, 16), (64, 128, 16), (300, 1, 16), (2048, 128, 64)])
 def test_logits_full_vocab(oracle, M, thr, n_rows):
     """Odd-vocab logits (K=5120, n_stored=248320, n_gemm=248192,
     n_decodable=248077, bits=6) at M = 1, 16 (the 16-row decode kernel), 64
@@ -424,8 +459,10 @@ MASK_PATHS = {
     "decode_whole_block": dict(K=128, n_stored=248320, n_gemm=248192, bits=6, M=3, thr=0),
     # tensor-core decode kernel (16 < M), its slot reduction
     "fused_decode": dict(K=256, n_stored=640, n_gemm=512, bits=6, M=40, thr=0),
-    # prefill GEMM: whole-tile epilogue over two reconstruct chunks
-    "prefill_epilogue": dict(K=256, n_stored=33408, n_gemm=33152, bits=4, M=256, thr=1),
+    # prefill GEMM: whole-tile epilogue over two reconstruct chunks (M > 512)
+    "prefill_epilogue": dict(K=256, n_stored=33408, n_gemm=33152, bits=4, M=520, thr=1),
+    # fused prefill (one 512-row block, many column blocks): its TMEM epilogue
+    "fused_prefill": dict(K=256, n_stored=33408, n_gemm=33152, bits=4, M=300, thr=1),
     # prefill GEMM: last partial wave split along K, reduced by its finalize kernel
     "prefill_split_tail": dict(K=2048, n_stored=512, n_gemm=384, bits=4, M=6, thr=1),
 }

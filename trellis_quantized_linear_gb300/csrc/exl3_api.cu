@@ -34,6 +34,18 @@ bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr
 
 exl3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA; }
 
+// The fused prefill kernel (decode in producer warps, one 512-row block) is
+// used where it was measured faster than reconstruct + GEMM: a single
+// 512-row block (it decodes W once, as the reconstruct does, but writes no
+// W^T) over enough 256-column blocks to keep most CTA pairs busy. Gate
+// geometry (5120 -> 17408, 68 column blocks): 66.8 vs 86.5 us at M = 256,
+// 83.0 vs 108.1 us at M = 512; at M = 768 and up, and on the down geometry
+// (20 column blocks), reconstruct + GEMM wins.
+bool fused_prefill_pays(int64_t M, int64_t n_gemm, int num_sms) {
+  const int64_t col_blocks = (n_gemm + 255) / 256;
+  return M <= 512 && 10 * col_blocks >= 3 * (int64_t)num_sms;
+}
+
 // Shared by exl3_linear and exl3_logits_masked once arguments are validated.
 exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const void *x, int64_t M, int64_t K,
                        const uint16_t *trellis, int bits, int64_t n_stored, int64_t n_gemm, int64_t n_valid,
@@ -96,6 +108,24 @@ exl3_status run_linear(const DeviceInfo *dev, const WorkspaceLayout &L, const vo
   void *wchunk = ws + L.wchunk_off;
   cudaError_t e = launch_hadamard128(x, xr, su, M, K, dev->num_sms, st);
   if (e != cudaSuccess) return EXL3_ERR_CUDA;
+  if (fused_prefill_pays(M, n_gemm, dev->num_sms)) {
+    FusedPrefillLaunch f;
+    f.xr = xr;
+    f.xr_rows = L.xr_rows;
+    f.M = M;
+    f.K = K;
+    f.trellis = trellis;
+    f.bits = bits;
+    f.n_stored = n_stored;
+    f.n_gemm = n_gemm;
+    f.n_valid = n_valid;
+    f.sv = sv;
+    f.y = y;
+    f.y_f32 = y_dtype == EXL3_F32;
+    f.status = dev->status;
+    f.num_sms = dev->num_sms;
+    return launch_fused_prefill(f, st) == cudaSuccess ? EXL3_OK : EXL3_ERR_CUDA;
+  }
   for (int64_t c0 = 0; c0 < n_gemm; c0 += EXL3_RECONSTRUCT_CHUNK_COLS) {
     const int64_t nc = (n_gemm - c0) < EXL3_RECONSTRUCT_CHUNK_COLS ? (n_gemm - c0) : EXL3_RECONSTRUCT_CHUNK_COLS;
     // The first chunk may run alongside the input rotation (independent
@@ -217,7 +247,7 @@ exl3_status exl3_init(int device) {
   if (init_rotate_kernels(info.status) != cudaSuccess || init_reconstruct_kernels(info.status) != cudaSuccess ||
       init_reconstruct_rotated_kernels(info.status) != cudaSuccess ||
       init_decode_kernels(info.status) != cudaSuccess || init_prefill_kernels(info.status) != cudaSuccess ||
-      init_fused_kernels(info.status) != cudaSuccess)
+      init_fused_kernels(info.status) != cudaSuccess || init_fused_prefill_kernels(info.status) != cudaSuccess)
     return EXL3_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return EXL3_ERR_CUDA;
   info.ready = true;
@@ -435,7 +465,8 @@ exl3_status exl3_selftest_bounds(int *units_reported, int *units_total, void *st
   if (pending != EXL3_OK) return pending;
   cudaError_t (*const probes[])(cudaStream_t) = {bounds_probe_rotate,  bounds_probe_decode,
                                                  bounds_probe_fused,   bounds_probe_prefill,
-                                                 bounds_probe_reconstruct, bounds_probe_reconstruct_rotated};
+                                                 bounds_probe_reconstruct, bounds_probe_reconstruct_rotated,
+                                                 bounds_probe_fused_prefill};
   for (auto *probe : probes) {
     ++*units_total;
     if (probe(st) != cudaSuccess) return EXL3_ERR_CUDA;

@@ -106,10 +106,27 @@ struct FusedLaunch {
   FusedPlan plan;
 };
 
+// Fused prefill-shaped layer (decode in producer warps, CTA pairs, 512 x 256
+// tiles): y = had_r_128(x' . W) * sv with the -inf mask past n_valid.
+struct FusedPrefillLaunch {
+  const void *xr;          // rotated rows (fp16), ld = K
+  int64_t xr_rows, M, K;   // xr_rows >= M rounded up to 128
+  const uint16_t *trellis;
+  int bits;
+  int64_t n_stored, n_gemm, n_valid;
+  const void *sv;
+  void *y;                 // M x n_gemm
+  int y_f32;
+  int *status;
+  int num_sms;
+};
+
 // Each kernel translation unit's set-up; `status` is the device error word
 // (bound into the unit's bounds checks in the bounds-checked build).
 cudaError_t init_rotate_kernels(int *status);
 cudaError_t init_fused_kernels(int *status);
+cudaError_t init_fused_prefill_kernels(int *status);
+cudaError_t launch_fused_prefill(const FusedPrefillLaunch &p, cudaStream_t st);
 cudaError_t launch_fused_gemm(const FusedLaunch &p, cudaStream_t st);
 // Sums the partial slots of shared n-blocks (slot order), output rotation,
 // sv, mask, store. Units are k slabs (decode GEMM) or k steps (fused GEMM).
@@ -129,6 +146,7 @@ cudaError_t init_prefill_kernels(int *status);
 cudaError_t bounds_probe_rotate(cudaStream_t st);
 cudaError_t bounds_probe_decode(cudaStream_t st);
 cudaError_t bounds_probe_fused(cudaStream_t st);
+cudaError_t bounds_probe_fused_prefill(cudaStream_t st);
 cudaError_t bounds_probe_prefill(cudaStream_t st);
 cudaError_t bounds_probe_reconstruct(cudaStream_t st);
 cudaError_t bounds_probe_reconstruct_rotated(cudaStream_t st);
