@@ -218,11 +218,15 @@ exl3_status exl3_linear_weight_rotated(const void *x, int64_t M, int64_t K, cons
  *          kernel with the decoded weights as the mma.sync operand; for
  *          larger M one tensor-core (tcgen05) kernel per 256 rows whose
  *          producer warps decode straight into the MMA operand buffers.
- *          Otherwise the prefill-shaped path runs had_r_128 -> reconstruct
- *          (32768-column chunks into the workspace) -> tensor-core GEMM with
- *          the output rotation fused in its epilogue. On one GB300 the
- *          prefill-shaped path is faster from M = 768 (4-bit 5120 -> 17408)
- *          and from M = 1024 (4-bit 17408 -> 5120).
+ *          Otherwise the prefill-shaped path runs had_r_128, then either
+ *          (M <= 512 on a layer with at least 0.3 x SMs column blocks of
+ *          256) one fused tensor-core kernel whose producer warps decode
+ *          straight into the MMA operand, 512 rows per decoded tile, or
+ *          reconstruct (32768-column chunks into the workspace) followed by
+ *          a tensor-core GEMM; both apply the output rotation, sv and the
+ *          mask in their epilogue. On one GB300 the prefill-shaped path is
+ *          faster from M = 384 (4-bit 5120 -> 17408) and from M = 768
+ *          (4-bit 17408 -> 5120).
  *   workspace: device buffer of at least
  *          exl3_linear_workspace_bytes(M, K, n_gemm, bits, m_threshold)
  *          bytes, cleared once by exl3_workspace_init. Calls that share a
