@@ -18,9 +18,11 @@
 //     CTAs' bytes complete on the even CTA's stage barrier;
 //   * warps 2..17 of each CTA (decoders): this CTA's 128-column n-block of
 //     W^T, decoded into the N operand (K-major, 128-byte swizzle), four warps
-//     per k step, each a 16-row slab streamed through a private bulk-copy
-//     ring (the operand-row permutation of the decode-shaped fused kernel:
-//     column 16g + c at operand row 16g + (c ^ g));
+//     per k step, each a 16-row slab whose trellis words every lane loads
+//     from global memory one slab ahead, into registers (no shared-memory
+//     ring: that room goes to a fourth x' stage); the operand-row
+//     permutation of the decode-shaped fused kernel: column 16g + c at
+//     operand row 16g + (c ^ g);
 //   * warp 1 of the even CTA (one lane): two tcgen05.mma.cta_group::2 chains
 //     (M = 256 rows, N = 256 columns, K = 16): sub-block j into TMEM columns
 //     256 j .. 256 j + 255 of both CTAs (TMEM lane = row, column = output
@@ -54,26 +56,23 @@ constexpr int FP_DEC_WARPS = 16, FP_EPI_WARPS = 4;
 constexpr int FP_GROUPS = FP_DEC_WARPS / 4;  // k steps decoded concurrently (4 slabs each)
 constexpr int FP_THREADS = (2 + FP_DEC_WARPS + FP_EPI_WARPS) * 32;
 constexpr int FP_SUB = 128 * FP_BK * 2;      // 128 rows x 64 fp16 (an x' sub-block half or a W^T n-block)
-constexpr int FP_RD = 2;                     // trellis slabs in flight per decoder warp
 constexpr int FP_TMEM_COLS = 512;
 constexpr uint32_t kIdescFP = f16_idesc(256, 256);
 
 template <int BITS>
 struct FPCfg {
-  static constexpr int kSeg = 256 * BITS;  // trellis bytes of one 16-row slab of an n-block
-  static constexpr int kRings = FP_DEC_WARPS * FP_RD * kSeg;
-  static constexpr int kRest = 227 * 1024 - 2048 - 1024 - kRings;
-  // x' stages (two 16 KB halves each): three when at least five W^T stages
-  // still fit, else two.
-  static constexpr int kSA = (kRest - 3 * 2 * FP_SUB) / FP_SUB >= FP_GROUPS + 1 ? 3 : 2;
+  static constexpr int kRest = 227 * 1024 - 2048 - 1024;
+  // x' stages (two 16 KB halves each): four, leaving room for five W^T
+  // stages (the least the four decoder groups need).
+  static constexpr int kSA = (kRest - (FP_GROUPS + 1) * FP_SUB) / (2 * FP_SUB) > 4
+                                 ? 4 : (kRest - (FP_GROUPS + 1) * FP_SUB) / (2 * FP_SUB);
   // W^T stages: with 2 * FP_GROUPS a decoder group only needs the stage the
   // MMA was handed a whole round earlier; as many as fit, up to that.
   static constexpr int kSBFit = (kRest - kSA * 2 * FP_SUB) / FP_SUB;
   static constexpr int kSB = kSBFit > 2 * FP_GROUPS ? 2 * FP_GROUPS : kSBFit;
   static constexpr int kOffB = kSA * 2 * FP_SUB;
-  static constexpr int kOffD = kOffB + kSB * FP_SUB;
-  static constexpr int kOffBar = kOffD + kRings;
-  static constexpr int kNumBars = 2 * kSA + 2 * kSB + 3 + FP_DEC_WARPS * FP_RD;
+  static constexpr int kOffBar = kOffB + kSB * FP_SUB;
+  static constexpr int kNumBars = 2 * kSA + 2 * kSB + 3;
   // barriers and the TMEM slot, then the current tile's 256 sv values
   static constexpr int kOffSv = kOffBar + 512;
   static constexpr int kSmem = 2048 + kOffSv + 512;
@@ -188,7 +187,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
   const uint32_t acc_full = smem_u32(&bars[2 * SA + 2 * SB]);
   const uint32_t acc_empty = smem_u32(&bars[2 * SA + 2 * SB + 1]);
   const uint32_t done_bar = smem_u32(&bars[2 * SA + 2 * SB + 2]);
-  auto dec_full = [&](int w, int s) { return smem_u32(&bars[2 * SA + 2 * SB + 3 + w * FP_RD + s]); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBars);
   auto a_s = [&](int s, int j) { return smem_s + (uint32_t)(s * 2 * FP_SUB + j * FP_SUB); };
   auto b_s = [&](int s) { return smem_s + (uint32_t)(Cfg::kOffB + s * FP_SUB); };
@@ -219,8 +217,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * FP_EPI_WARPS);
     mbar_init(done_bar, 1);
-    for (int w = 0; w < FP_DEC_WARPS; ++w)
-      for (int s = 0; s < FP_RD; ++s) mbar_init(dec_full(w, s), 1);
     fence_barrier_init();
   }
   if (warp == 1) {  // one warp of each CTA of the pair allocates together
@@ -244,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
       for (int64_t z = 0; z < len; ++z) {
         const int tb = tile_tb(i);
         const int nsub = tb * 512 + 256 < p.M ? 2 : 1;
-        if (!mbar_wait_cluster(a_empty(as), aph ^ 1u, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(a_empty(as), aph ^ 1u, p.status)) break;
         if (rank == 0) mbar_arrive_expect_tx(a_full(as), (uint32_t)(2 * nsub * FP_SUB));
         const uint32_t fb = map_to_rank(a_full(as), 0);
         for (int j = 0; j < nsub; ++j) {
@@ -321,7 +317,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
     const int par = dw >> 2, slab_i = dw & 3;  // units par, par + FP_GROUPS, ...; slab slab_i of each
     const int g = lane >> 2, q = lane & 3;
     const int64_t nmine = len > par ? (len - par + FP_GROUPS - 1) / FP_GROUPS : 0;
-    const uint32_t ring_s = smem_s + Cfg::kOffD + dw * FP_RD * Cfg::kSeg;
     // Swizzled W^T address of (column 16g + c, rows 4q..4q+3 of slab slab_i)
     // = (stage + lane_off) ^ (c << 7 | (c & 7) << 4), stage 2048-byte aligned:
     // operand row t = c ^ g of 8-row atom 2g + (t >> 3), 16-byte chunk
@@ -329,10 +324,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
     const uint32_t lane_off = (uint32_t)g * 2048u | (uint32_t)g << 7 |
                               (((uint32_t)(2 * slab_i + (q >> 1)) ^ (uint32_t)g) & 7u) << 4 | (uint32_t)(q & 1) << 3;
     const int64_t nblk = p.n_gemm / 128;
-    int64_t issued = 0;
-    // Cursor of the next slab to fetch (tile i, k step ks); fetches go in order.
+    // Cursor of the next slab to load (tile i, k step ks); loads go in order.
     int fi = (int)(par / KS), fks = (int)(par % KS);
-    auto issue = [&](int64_t jj) {
+    // The lane's 8 * BITS bytes of the next slab, loaded into `w`.
+    auto load_next = [&](uint32_t (&w)[2 * BITS]) {
       // this CTA's n-block of the tile (the last real one for a 128-wide last
       // column block: decoded, never stored)
       int64_t nb = 2 * (int64_t)tile_cp(fi) + rank;
@@ -343,41 +338,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
         fks -= KS;
         ++fi;
       }
-      const int s = (int)(jj % FP_RD);
-      mbar_arrive_expect_tx(dec_full(dw, s), Cfg::kSeg);
       // the slab's 8 tiles: tile row tk of the 4 KS, tiles [8 nb, +8) of tiles_n
-      if (EXL3_RANGE(tk, 0, 4 * (int64_t)KS) && EXL3_SPAN(nb * 8, 8, p.tiles_n) &&
-          EXL3_ALIGNED((tk * p.tiles_n + nb * 8) * (32 * BITS), 16))
-        bulk_g2s(ring_s + s * Cfg::kSeg, p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS), Cfg::kSeg,
-                 dec_full(dw, s));
-      ++issued;
+      if (EXL3_RANGE(tk, 0, 4 * (int64_t)KS) && EXL3_SPAN(nb * 8, 8, p.tiles_n)) {
+        load_own_words<BITS, false>(p.trellis + (tk * p.tiles_n + nb * 8) * (32 * BITS) + lane * 8 * BITS, w);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2 * BITS; ++k) w[k] = 0;
+      }
     };
-    if (lane == 0)
-      for (int64_t jj = 0; jj < FP_RD - 1 && jj < nmine; ++jj) issue(jj);
+    uint32_t nxt[2 * BITS];
+    if (nmine > 0) load_next(nxt);
     int bs = par % SB;  // W^T stage of unit par + FP_GROUPS * j, and its phase
     uint32_t bph = 0;
     const uint32_t bf_leader0 = map_to_rank(b_full(0), 0);
-    // On a timeout the warp stops, but first waits (bounded) for the copies
-    // it still has in flight into its ring, in issue order.
-    auto drain_from = [&](int64_t u0) {
-      if (lane == 0)
-        for (int64_t u = u0; u < issued; ++u)
-          mbar_wait_short(dec_full(dw, (int)(u % FP_RD)), (uint32_t)(u / FP_RD) & 1u);
-    };
     for (int64_t jj = 0; jj < nmine; ++jj) {
-      if (lane == 0 && jj + FP_RD - 1 < nmine) issue(jj + FP_RD - 1);
-      const int s = (int)(jj % FP_RD);
-      if (!mbar_wait(dec_full(dw, s), (uint32_t)(jj / FP_RD) & 1u, p.status)) {
-        drain_from(jj);
-        break;
-      }
       uint32_t own[2 * BITS];
-      if (EXL3_SPAN(s * Cfg::kSeg + lane * 8 * BITS, 8 * BITS, FP_RD * Cfg::kSeg)) {
-        load_own_words_shared<BITS>(ring_s + s * Cfg::kSeg + lane * 8 * BITS, own);
-      } else {
 #pragma unroll
-        for (int k = 0; k < 2 * BITS; ++k) own[k] = 0;
-      }
+      for (int k = 0; k < 2 * BITS; ++k) own[k] = nxt[k];
+      if (jj + 1 < nmine) load_next(nxt);
       const uint32_t prev = prefix_from_neighbour<BITS>(own, lane);
       uint32_t st[4][16];
       if constexpr (BITS == 4) {
@@ -390,10 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
           static_for<16>([&](auto C) { st[R.value][C.value] = rw.template state<R.value, C.value>(); });
         });
       }
-      if (!mbar_wait_cluster(b_empty(bs), bph ^ 1u, p.status, kWaitLimitNs)) {
-        drain_from(jj + 1);
-        break;
-      }
+      if (!mbar_wait(b_empty(bs), bph ^ 1u, p.status)) break;
       const uint32_t bt = b_s(bs) + lane_off;  // low 11 bits: lane_off's
       static_for<16>([&](auto C) {
         constexpr int cc = C.value;
@@ -402,10 +377,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
         const uint32_t hi = decode_pair_sel<false>(st[2][cc], st[3][cc]);
         if (EXL3_RANGE(bs, 0, SB) && EXL3_SPAN((bt ^ cx) - b_s(bs), 8, FP_SUB)) st_shared_v2(bt ^ cx, lo, hi);
       });
-      // the generic stores, visible to the pair MMA (issued by the even CTA)
-      asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+      // The generic stores (to this CTA's shared memory), visible to the
+      // tensor core; then the stage's arrival on the even CTA's barrier:
+      // local there, remote (release at cluster scope) from the odd CTA.
+      fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bf_leader0 + 8u * (uint32_t)bs);
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(b_full(bs)); else mbar_arrive_cluster(bf_leader0 + 8u * (uint32_t)bs);
+      }
       bs += FP_GROUPS;
       if (bs >= SB) {
         bs -= SB;
@@ -427,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
       // stop after a timed-out wait the same in all four warps.
       const int64_t col = (int64_t)cp * 256 + 2 * et;
       const uint32_t v = col < p.n_gemm ? __ldg(reinterpret_cast<const uint32_t *>(p.sv + col)) : 0u;
-      const uint32_t ok = mbar_wait_cluster(acc_full, (uint32_t)i & 1u, p.status, kWaitLimitNs) ? 1u : 0u;
+      const uint32_t ok = mbar_wait(acc_full, (uint32_t)i & 1u, p.status) ? 1u : 0u;
       uint32_t all_ok;
       asm volatile(
           "{\n\t.reg .pred p, q;\n\t"
