@@ -16,7 +16,7 @@
 //   * warp 0 (one lane) of each CTA: TMA loads of this CTA's 128 rows of each
 //     of the tile's two 256-row sub-blocks of x' (128-byte swizzle); both
 //     CTAs' bytes complete on the even CTA's stage barrier;
-//   * warps 2..17 of each CTA (decoders): this CTA's 128-column n-block of
+//   * warps 2..13 of each CTA (decoders): this CTA's 128-column n-block of
 //     W^T, decoded into the N operand (K-major, 128-byte swizzle), four warps
 //     per k step, each a 16-row slab whose trellis words every lane loads
 //     from global memory one slab ahead, into registers (no shared-memory
@@ -27,8 +27,9 @@
 //     (M = 256 rows, N = 256 columns, K = 16): sub-block j into TMEM columns
 //     256 j .. 256 j + 255 of both CTAs (TMEM lane = row, column = output
 //     column in operand order);
-//   * warps 18..21 of each CTA (epilogue): after the tile's last k step, per
-//     row and 128-column block, had_r_128 as a 32-point transform of each
+//   * warps 14..21 of each CTA (epilogue, two per TMEM lane group, one per
+//     128-column half): after the tile's last k step, per row and
+//     128-column block, had_r_128 as a 32-point transform of each
 //     32-column chunk (written back to TMEM in output order) followed by a
 //     4-point transform across the chunks, then sv, the -inf mask and the
 //     store. The stages run in the order h = 1, 2, ..., 64 with the same
@@ -52,7 +53,10 @@ namespace exl3 {
 namespace {
 
 constexpr int FP_BK = 64;
-constexpr int FP_DEC_WARPS = 16, FP_EPI_WARPS = 4;
+// 12 decoder warps keep ahead of the MMA (they wait for free W^T stages most
+// of the time); 8 epilogue warps (two per TMEM lane group, one per 128-column
+// half) halve the single-buffered accumulator's drain.
+constexpr int FP_DEC_WARPS = 12, FP_EPI_WARPS = 8;
 constexpr int FP_GROUPS = FP_DEC_WARPS / 4;  // k steps decoded concurrently (4 slabs each)
 constexpr int FP_THREADS = (2 + FP_DEC_WARPS + FP_EPI_WARPS) * 32;
 constexpr int FP_SUB = 128 * FP_BK * 2;      // 128 rows x 64 fp16 (an x' sub-block half or a W^T n-block)
@@ -394,18 +398,20 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
   } else {
     // ---------------- epilogue (both CTAs) ----------------
     const int lg = warp & 3;  // TMEM lane group this warp may access
+    const int ew = warp - 2 - FP_DEC_WARPS;  // 0 .. 7
+    const int h = ew >> 2;                   // the 128-column half this warp rotates
     const uint32_t ae = map_to_rank(acc_empty, 0);
     const uint32_t sv_s = smem_s + Cfg::kOffSv;
-    const int et = (warp - 2 - FP_DEC_WARPS) * 32 + lane;  // 0 .. 127
+    const int et = ew * 32 + lane;  // 0 .. 255
     for (int i = 0; i < my_tiles; ++i) {
       const int tb = tile_tb(i), cp = tile_cp(i);
       const int nsub = tb * 512 + 256 < p.M ? 2 : 1;
-      // The tile's sv columns 256 cp + 2 et, +1 go to shared memory once
-      // every epilogue thread has its accumulator (and is done with the
-      // previous tile's sv). The named barrier also makes the decision to
-      // stop after a timed-out wait the same in all four warps.
-      const int64_t col = (int64_t)cp * 256 + 2 * et;
-      const uint32_t v = col < p.n_gemm ? __ldg(reinterpret_cast<const uint32_t *>(p.sv + col)) : 0u;
+      // The tile's sv column 256 cp + et goes to shared memory once every
+      // epilogue thread has its accumulator (and is done with the previous
+      // tile's sv). The named barrier also makes the decision to stop after
+      // a timed-out wait the same in all eight warps.
+      const int64_t col = (int64_t)cp * 256 + et;
+      const uint32_t v = col < p.n_gemm ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p.sv + col)) : 0u;
       const uint32_t ok = mbar_wait(acc_full, (uint32_t)i & 1u, p.status) ? 1u : 0u;
       uint32_t all_ok;
       asm volatile(
@@ -417,17 +423,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(80)
           : "r"(ok), "n"(FP_EPI_WARPS * 32)
           : "memory");
       if (!all_ok) break;
-      asm volatile("st.shared.u32 [%0], %1;" ::"r"(sv_s + 4u * (uint32_t)et), "r"(v) : "memory");
+      asm volatile("st.shared.u16 [%0], %1;" ::"r"(sv_s + 2u * (uint32_t)et), "h"((unsigned short)v) : "memory");
       asm volatile("bar.sync 1, %0;" ::"n"(FP_EPI_WARPS * 32) : "memory");
       tc_fence_after();
+      const int64_t col0 = (int64_t)cp * 256 + 128 * h;
       for (int j = 0; j < nsub; ++j) {
         const int64_t row = (int64_t)tb * 512 + 256 * j + 128 * (int)rank + lg * 32 + lane;
-        for (int h = 0; h < 2; ++h) {
-          const int64_t col0 = (int64_t)cp * 256 + 128 * h;
-          if (col0 < p.n_gemm)
-            fp_epilogue_block(tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(256 * j + 128 * h), p, row, col0,
-                              sv_s + 256u * (uint32_t)h);
-        }
+        if (col0 < p.n_gemm)
+          fp_epilogue_block(tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(256 * j + 128 * h), p, row, col0,
+                            sv_s + 256u * (uint32_t)h);
       }
       tc_fence_before();
       __syncwarp();
