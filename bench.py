@@ -72,7 +72,7 @@ def parse_args():
     p.add_argument("--profile-call", default=None, metavar="K,N,BITS,M[,REPS[,THRESHOLD]]",
                    help="profiling aid: run exl3_linear REPS (default 4) times on one seeded matrix of that shape "
                         "with that m_threshold (default 0: decode-shaped) and exit (no JSON line)")
-    p.add_argument("--extras", default="prefill,crossover,logits,mlp_stack,decode_stack",
+    p.add_argument("--extras", default="prefill,prefill_fused,crossover,logits,mlp_stack,decode_stack",
                    help="comma-separated sub-measurements to run after the headline")
     return p.parse_args()
 
@@ -557,6 +557,34 @@ def bench_prefill(args, torch, tql, peaks):
             "cpu_baseline": oracle_line(t_call, cpu)}
 
 
+def bench_prefill_fused(args, torch, tql, peaks):
+    """Prefill-shaped gate_proj at M=512, the largest M at which exl3_linear
+    takes the fused prefill kernel (the trellis decoded into the MMA operand,
+    no reconstructed weight). Graph replays over distinct weight copies (more
+    than 4x L2 in total), whole call including the input rotation."""
+    K, N, bits, M = 5120, 17408, 4, 512
+    nc = copies_for(K * N * bits // 8)
+    mats = [DevMatrix(torch, synthetic.make_matrix(K, N, bits, seed=synthetic.PREFILL_SEED, matrix_index=j))
+            for j in range(nc)]
+    x = _dev(torch, synthetic.make_activations(M, K, seed=synthetic.PREFILL_SEED))
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = make_ws(torch, tql, M, K, N, bits, 128)
+    reps = 2 if args.quick else 5
+    t_call = graph_time(torch, [lambda m=m: call_linear(tql, x, M, m, y, 128, ws, tql.EXL3_F16) for m in mats], reps)
+    nbytes = mats[0].nbytes
+    del mats
+    flops = 2.0 * M * K * N
+    tflops = flops / (t_call * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    cpu = oracle_call_time(K, N, bits, M, synthetic.PREFILL_SEED, rows=128)
+    return {"geometry": "K=5120 N=17408 bits=4 M=512", "path": "fused prefill (decode into the MMA operand)",
+            "ms_per_call": round(t_call, 4), "tflops": round(tflops, 1), "peak_tflops": peak,
+            "frac": round(tflops / peak, 4),
+            "peak_kind": f"of {peaks['source']} (cuBLAS bf16 burst; fp16 same rate)",
+            "timing": f"CUDA graph replays over {nc} weight copies ({nc * nbytes / 1e6:.0f} MB > 4x L2)",
+            "cpu_baseline": oracle_line(t_call, cpu)}
+
+
 def bench_crossover(args, torch, tql):
     """Both paths at every M on both MLP geometries. Each (M, path) time
     replays a CUDA graph of calls over distinct weight copies (> 4x L2 in
@@ -931,6 +959,7 @@ def main():
     if not args.no_extras and rank == 0:
         wanted = set(args.extras.split(","))
         for name, fn in (("prefill", lambda: bench_prefill(args, torch, tql, peaks)),
+                         ("prefill_fused", lambda: bench_prefill_fused(args, torch, tql, peaks)),
                          ("crossover", lambda: bench_crossover(args, torch, tql)),
                          ("logits", lambda: bench_logits(args, torch, tql, peaks)),
                          ("mlp_stack", lambda: bench_mlp_stack(args, torch, tql, peaks)),
