@@ -122,6 +122,20 @@ int64_t exl3_aligned_logits_width(int64_t n_decodable, int64_t n_stored);
 int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *ctas_per_split);
 
 /*
+ * The kernels a prefill-shaped call (m_threshold > 0 and M >= m_threshold)
+ * of M rows takes on a layer n_gemm columns wide, on a GPU with `num_sms`
+ * SMs: 1 for the fused prefill kernel, whose producer warps decode the
+ * trellis straight into the tensor-core operand (the "dequant fused into
+ * the GEMM" of [P1] "The remaining gap is structural"), used for
+ * M <= 512 on layers with at least 0.3 x num_sms column blocks of 256; 0 for
+ * reconstruct (32768-column chunks) followed by the tensor-core GEMM.
+ * Both apply the input and output rotations, sv and the logits mask.
+ * Returns -1 on invalid input (M < 1, n_gemm not a positive multiple of
+ * 128, num_sms < 1). Host only.
+ */
+int exl3_prefill_path(int64_t M, int64_t n_gemm, int num_sms);
+
+/*
  * Workspace bytes an exl3_linear / exl3_logits_masked call with M <= M_max
  * needs on a GPU with `num_sms` streaming multiprocessors. The workspace is
  * laid out as: split-K partial sums (shared by the decode-shaped kernels

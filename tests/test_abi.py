@@ -129,6 +129,21 @@ def test_decode_plan_invariants(lib, K, N, sms):
     assert z[0] == 0 and z[-1] == TS and all(b > a for a, b in zip(z, z[1:]))
 
 
+@pytest.mark.parametrize("M,N,sms,want", [
+    (512, 17408, 152, 1), (513, 17408, 152, 0), (1, 17408, 152, 1),   # gate: up to one 512-row block
+    (512, 5120, 152, 0),                                               # down: 20 column blocks
+    (300, 248192, 152, 1),                                             # odd-vocab logits
+    (256, 11776, 152, 1), (256, 11520, 152, 0),                        # 46 / 45 column blocks of 256
+    (256, 11520, 148, 1),                                              # the rule scales with the SM count
+    (0, 512, 152, -1), (512, 100, 152, -1), (512, 512, 0, -1),         # invalid
+])
+def test_prefill_path_rule(lib, M, N, sms, want):
+    """The prefill-shaped side takes the fused prefill kernel for at most 512
+    rows on layers with at least 0.3 x SMs column blocks of 256 (where it was
+    measured faster), else reconstruct + GEMM."""
+    assert tql.exl3_prefill_path(M, N, sms) == want
+
+
 def test_decode_plan_gate_geometry_fills_every_sm(lib):
     slots, ctas = tql.exl3_decode_plan(5120, 17408, 152)
     assert ctas == 152 and slots == 15

@@ -20,7 +20,7 @@ import threading
 __all__ = [
     "Exl3Error", "build", "load", "EXL3_F16", "EXL3_F32", "EXL3_LAYOUT_KN", "EXL3_LAYOUT_NK",
     "EXL3_RECONSTRUCT_CHUNK_COLS", "EXL3_NOALLOC_SCRATCH_BYTES", "exl3_init", "exl3_status_string", "exl3_supported_bits",
-    "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_linear_workspace_bytes_for",
+    "exl3_aligned_logits_width", "exl3_decode_plan", "exl3_prefill_path", "exl3_linear_workspace_bytes_for",
     "exl3_linear_workspace_bytes", "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct",
     "exl3_linear", "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
     "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
@@ -48,7 +48,7 @@ STATUS_NAMES = {
 # Every function include/exl3.h declares.
 HEADER_SYMBOLS = (
     "exl3_init", "exl3_status_string", "exl3_supported_bits", "exl3_aligned_logits_width",
-    "exl3_decode_plan", "exl3_linear_workspace_bytes_for", "exl3_linear_workspace_bytes",
+    "exl3_decode_plan", "exl3_prefill_path", "exl3_linear_workspace_bytes_for", "exl3_linear_workspace_bytes",
     "exl3_workspace_init", "exl3_hadamard128", "exl3_reconstruct", "exl3_linear",
     "exl3_logits_masked", "exl3_get_device_status", "exl3_selftest_wait_timeout",
     "exl3_linear_decode_noalloc", "exl3_silu_mul", "exl3_reconstruct_rotated",
@@ -93,6 +93,7 @@ def load():
             "exl3_aligned_logits_width": (_i64, [_i64, _i64]),
             "exl3_decode_plan": (ctypes.c_int, [_i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                                 ctypes.POINTER(ctypes.c_int)]),
+            "exl3_prefill_path": (ctypes.c_int, [_i64, _i64, ctypes.c_int]),
             "exl3_linear_workspace_bytes_for": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int, _i64, ctypes.c_int]),
             "exl3_linear_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int, _i64]),
             "exl3_workspace_init": (ctypes.c_int, [_vp, ctypes.c_size_t, _vp]),
@@ -175,6 +176,12 @@ def exl3_decode_plan(K: int, n_gemm: int, num_sms: int):
     if rc != 0:
         raise ValueError("exl3_decode_plan: invalid geometry")
     return s.value, g.value
+
+
+def exl3_prefill_path(M: int, n_gemm: int, num_sms: int) -> int:
+    """1: a prefill-shaped call of M rows on an n_gemm-wide layer takes the
+    fused prefill kernel; 0: reconstruct + GEMM; -1: invalid input."""
+    return int(load().exl3_prefill_path(int(M), int(n_gemm), int(num_sms)))
 
 
 def exl3_linear_workspace_bytes_for(M_max, K, n_gemm, bits, m_threshold, num_sms) -> int:

@@ -289,6 +289,11 @@ int exl3_decode_plan(int64_t K, int64_t n_gemm, int num_sms, int *splits, int *c
   return 0;
 }
 
+int exl3_prefill_path(int64_t M, int64_t n_gemm, int num_sms) {
+  if (M < 1 || n_gemm <= 0 || n_gemm % 128 || num_sms < 1) return -1;
+  return fused_prefill_pays(M, n_gemm, num_sms) ? 1 : 0;
+}
+
 size_t exl3_linear_workspace_bytes_for(int64_t M_max, int64_t K, int64_t n_gemm, int bits, int64_t m_threshold,
                                        int num_sms) {
   WorkspaceLayout L;
