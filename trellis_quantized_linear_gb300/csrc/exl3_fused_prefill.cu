@@ -37,10 +37,12 @@
 // The accumulator takes all 512 TMEM columns, so the next tile's MMAs wait
 // for the epilogue; the decoders and the x' producer run ahead meanwhile.
 //
-// Roofline: per SM, 128 x 256 x 2 MACs per k step and 128 x 64 weights
-// decoded per k step: tensor-bound when the decoders keep 8 weights per
-// clock per SM. HBM: the trellis is read once per 512 rows (from L2 after
-// the first tile that needs it), x' once per 256 output columns.
+// Roofline: per SM and k step, 128 x 256 x 2 MACs (about 1050 cycles of
+// tensor work) and 128 x 64 weights decoded (8 a cycle keep up); HBM: the
+// trellis read once per 512 rows, x' once per 256 output columns. Measured,
+// a k step takes about 1.5x its tensor work with the decoders well ahead;
+// the shared-memory traffic (about 112 KB per SM per k step of TMA writes,
+// decoder writes and operand reads) is the likely bound.
 #include <cuda.h>
 #include <math.h>
 
