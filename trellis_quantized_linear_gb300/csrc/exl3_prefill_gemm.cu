@@ -10,14 +10,20 @@
 //
 // A = x' (rotated activations, rows x K fp16, K-major) and B = W^T (the
 // reconstructed chunk, nc x K fp16, K-major) are staged by TMA with 128-byte
-// swizzle into a 4-stage ring; one thread issues tcgen05.mma (M=128, N=256,
-// K=16, fp32 accumulation in TMEM); the accumulator is double-buffered in
-// TMEM (2 x 256 columns) so the epilogue of tile i overlaps the main loop of
-// tile i+1. Persistent grid, one CTA per SM.
+// swizzle; tcgen05.mma accumulates in fp32 in TMEM, double-buffered (2 x 256
+// columns) so the epilogue of tile i overlaps the main loop of tile i+1.
+// Persistent grids, one CTA per SM. Two forms:
+//   * prefill_pair_kernel (from two 128-row tiles up): clusters of two CTAs
+//     share a 256 x 256 tile through tcgen05.mma.cta_group::2 (M=256, N=256),
+//     each CTA staging its 128 x' rows and half of the tile's W^T rows in a
+//     6-stage ring (32 KB per SM per 64-deep k block);
+//   * prefill_gemm_kernel (one 128-row tile, small problems, and the
+//     stream-K split of a short last wave): one CTA per 128 x 256 tile,
+//     tcgen05.mma M=128, N=256, a 4-stage ring (48 KB per k block).
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator
-// and MMA issuer, warps 2..5 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, i.e. one output row per thread).
+// and MMA issuer (the even CTA's, for a pair), warps 2..5 = epilogue (warp w
+// reads TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. one output row per thread).
 //
 // Roofline: tensor-bound, 2*M*K*nc flops per launch.
 #include <cuda.h>
