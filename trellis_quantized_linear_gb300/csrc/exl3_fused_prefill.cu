@@ -57,7 +57,7 @@ namespace {
 constexpr int FP_BK = 64;
 // 12 decoder warps keep ahead of the MMA (they wait for free W^T stages most
 // of the time); 8 epilogue warps (two per TMEM lane group, one per 128-column
-// half) halve the single-buffered accumulator's drain.
+// half) share the single-buffered accumulator's drain.
 constexpr int FP_DEC_WARPS = 12, FP_EPI_WARPS = 8;
 constexpr int FP_GROUPS = FP_DEC_WARPS / 4;  // k steps decoded concurrently (4 slabs each)
 constexpr int FP_THREADS = (2 + FP_DEC_WARPS + FP_EPI_WARPS) * 32;
